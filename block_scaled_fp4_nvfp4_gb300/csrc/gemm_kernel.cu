@@ -1,0 +1,506 @@
+// Persistent, warp-specialised NVFP4 block-scaled GEMM for sm_103a.
+//
+// One CTA per SM walks a static list of work units (output tile, K range) of
+// all groups.  Inside a CTA:
+//   warp 0      TMA producer: per 256-wide k-tile, one 3-D tensor copy each for
+//               the A tile (128 rows x 128 B) and the B tile (BN rows x 128 B)
+//               plus contiguous bulk copies of the scale atoms, all counted on
+//               the stage's "full" mbarrier;
+//   warp 1      MMA issuer (one thread): moves the k-tile's scale atoms into
+//               tensor memory with tcgen05.cp, issues four
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
+//               into a tensor-memory accumulator and commits the stage back;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one row per thread),
+//               fp32 -> fp16 (RNE), 128B-swizzled staging in shared memory and
+//               TMA tensor stores of 32 x 64 boxes (rows past M are clipped).
+// Split-K units write fp32 partials to a workspace; the last unit of a tile to
+// arrive sums all partials in split order (deterministic) and stores C.
+//
+// The warp roles and the mbarrier ring follow the structure of the pages'
+// kernels ("nvfp4 group gemm, submission 407526", grouped_kernel; "nvfp4 gemm,
+// submission 125598", kernel); the persistent unit loop, split-K, the
+// double-buffered accumulator, the scale-slot ring, the TMA-store epilogue and
+// the bounded waits are this library's own.
+//
+// Every wait is bounded (Waiter below).  When one runs out the CTA records a
+// status code, stops issuing, waits for its own copies and MMAs in flight,
+// frees its tensor memory and exits.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "descriptors.h"
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kMaxStages = 8;
+
+struct SmemCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t sf_free[8];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t epi_gather;
+  uint64_t epi_bcast;
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  int last_flag;
+};
+
+struct Unit {
+  int g, l, tm, tn, split, splits, kt0, kt1, tile;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
+  int g = 0;
+  while (g + 1 < p.num_groups && u >= p.unit_start[g + 1]) ++g;
+  const int r = u - p.unit_start[g];
+  const int S = p.splits[g];
+  Unit x;
+  x.g = g;
+  x.splits = S;
+  x.split = r % S;
+  const int t = r / S;  // tile index inside the group, m fastest
+  x.tm = t % p.tiles_m[g];
+  const int rest = t / p.tiles_m[g];
+  x.tn = rest % p.tiles_n[g];
+  x.l = rest / p.tiles_n[g];
+  const int KT = p.ktiles[g];
+  x.kt0 = static_cast<int>(static_cast<long long>(KT) * x.split / S);
+  x.kt1 = static_cast<int>(static_cast<long long>(KT) * (x.split + 1) / S);
+  x.tile = p.tile_start[g] + t;
+  return x;
+}
+
+// Bounded mbarrier wait.  Returns false if the CTA is aborting or the limit
+// ran out (then the abort flag and the device status word are set).
+struct Waiter {
+  volatile int* abort_flag;
+  int* status;
+  unsigned long long timeout_ns;
+
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int code) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t i = 1;; ++i) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if ((i & 7u) == 0) {
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > timeout_ns) {
+          *abort_flag = 1;
+          atomicCAS(status, 0, code);
+          return false;
+        }
+      }
+    }
+  }
+
+  // Used only while shutting down after an abort: waits for the CTA's own
+  // asynchronous work, bounded by the same limit, ignoring the abort flag.
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+      if (ptx::globaltimer() - t0 > timeout_ns) return false;
+    }
+    return true;
+  }
+};
+
+// Lane 0 waits, the result is broadcast, the warp reconverges.
+__device__ __forceinline__ bool warp_wait(const Waiter& W, uint32_t bar, uint32_t parity, int code) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = W.wait(bar, parity, code);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+}  // namespace
+
+template <int BN>
+__global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Cfg = TileCfg<BN>;
+  constexpr int kStages = Cfg::kStages;
+  static_assert(kStages <= kMaxStages, "stage ring too deep");
+
+  extern __shared__ uint8_t dsmem_raw[];
+  __shared__ SmemCtl ctl;
+
+  const uint32_t raw = ptx::smem_addr(dsmem_raw);
+  const uint32_t smem_base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024-B alignment
+  const uint32_t epi_base = smem_base + kStages * Cfg::kStageBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  auto full_bar = [&](int s) { return ptx::smem_addr(&ctl.full[s]); };
+  auto empty_bar = [&](int s) { return ptx::smem_addr(&ctl.empty[s]); };
+  auto sf_free_bar = [&](int s) { return ptx::smem_addr(&ctl.sf_free[s]); };
+  auto acc_full_bar = [&](int b) { return ptx::smem_addr(&ctl.acc_full[b]); };
+  auto acc_empty_bar = [&](int b) { return ptx::smem_addr(&ctl.acc_empty[b]); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < Cfg::kSfSlots; ++s) ptx::mbar_init(sf_free_bar(s), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(acc_full_bar(b), 1);
+      ptx::mbar_init(acc_empty_bar(b), kEpiWarps);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl.epi_gather), kEpiWarps);
+    ptx::mbar_init(ptx::smem_addr(&ctl.epi_bcast), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl.mma_drain), 1);
+    ctl.abort = 0;
+    ctl.last_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.num_groups; ++g) {
+      ptx::prefetch_tensormap(&p.tmA[g]);
+      ptx::prefetch_tensormap(&p.tmB[g]);
+      ptx::prefetch_tensormap(&p.tmC[g]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), Cfg::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+
+  const Waiter W{&ctl.abort, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_stream = ptx::policy_evict_first();
+      const uint64_t pol_keep = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) armed[s] = -1;
+      int count = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+        const Unit x = decode_unit(p, u);
+        const CUtensorMap* mapA = &p.tmA[x.g];
+        const CUtensorMap* mapB = &p.tmB[x.g];
+        const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
+        const uint64_t polB = p.a_streams[x.g] ? pol_keep : pol_stream;
+        const size_t atoms_per_block = static_cast<size_t>(p.ktiles[x.g]) * 4;
+        const uint8_t* sfa = p.sfa[x.g] +
+            (static_cast<size_t>(x.l) * p.sf_rows_a[x.g] + x.tm) * atoms_per_block * kSfAtomBytes;
+        const int sfb_block0 = x.tn * Cfg::kSfbBlocks;
+        const uint8_t* sfb = p.sfb[x.g] +
+            (static_cast<size_t>(x.l) * p.sf_rows_b[x.g] + sfb_block0) * atoms_per_block * kSfAtomBytes;
+        int nsfb = p.sf_rows_b[x.g] - sfb_block0;
+        nsfb = nsfb < Cfg::kSfbBlocks ? nsfb : Cfg::kSfbBlocks;
+        const uint32_t stage_tx =
+            Cfg::kABytes + Cfg::kBBytes + kSfSlabBytes + static_cast<uint32_t>(nsfb) * kSfSlabBytes;
+        for (int kt = x.kt0; kt < x.kt1; ++kt) {
+          if (!W.wait(empty_bar(stage), phase ^ 1u, kStatusTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sB = sA + Cfg::kABytes;
+          const uint32_t sSFA = sB + Cfg::kBBytes;
+          const uint32_t sSFB = sSFA + kSfSlabBytes;
+          if (blockIdx.x == 0 && count == p.debug_skip_ktile) {
+            armed[stage] = -1;  // test-only: nothing issued, nothing in flight
+          } else {
+            const uint32_t fb = full_bar(stage);
+            ptx::mbar_arrive_expect_tx(fb, stage_tx);
+            ptx::tma_load_3d(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
+            ptx::tma_load_3d(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
+            ptx::bulk_load(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
+            for (int j = 0; j < nsfb; ++j)
+              ptx::bulk_load(sSFB + j * kSfSlabBytes,
+                             sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
+                             kSfSlabBytes, fb, polB);
+            armed[stage] = static_cast<int>(phase);
+          }
+          ++count;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Shutting down: wait for the copies this thread put in flight.
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+          if (armed[s] >= 0) W.drain(full_bar(s), static_cast<uint32_t>(armed[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_nvf4(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+        const Unit x = decode_unit(p, u);
+        if (!W.wait(acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + ab * BN;
+        for (int kt = x.kt0; kt < x.kt1; ++kt) {
+          if (!W.wait(full_bar(stage), phase, kStatusTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          const int slot = it % Cfg::kSfSlots;
+          const int use = it / Cfg::kSfSlots;
+          if (use > 0 && !W.wait(sf_free_bar(slot), static_cast<uint32_t>(use - 1) & 1u, kStatusTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sB = sA + Cfg::kABytes;
+          const uint32_t sSFA = sB + Cfg::kBBytes;
+          const uint32_t sSFB = sSFA + kSfSlabBytes;
+          const uint32_t sfa_t = tmem + Cfg::kSfBaseCol + slot * Cfg::kSfSlotCols;
+          const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          // Scale atoms -> tensor memory.  Atom kb of a 128-row block holds
+          // the 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
+#pragma unroll
+          for (int kb = 0; kb < kBK / kMmaK; ++kb) {
+            ptx::tc_copy_sf(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+#pragma unroll
+            for (int j = 0; j < Cfg::kSfbBlocks; ++j)
+              ptx::tc_copy_sf(sfb_t + kb * (BN / 32) + 4 * j,
+                              scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes));
+          }
+#pragma unroll
+          for (int kb = 0; kb < kBK / kMmaK; ++kb) {
+            // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
+            ptx::tc_mma_nvf4(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
+                             sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
+                             (kt > x.kt0 || kb > 0) ? 1u : 0u);
+          }
+          ptx::tc_commit(empty_bar(stage));
+          ptx::tc_commit(sf_free_bar(slot));
+          ++it;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(acc_full_bar(ab));
+        if (++ab == Cfg::kAccBufs) {
+          ab = 0;
+          aphase ^= 1u;
+        }
+      }
+      if (!ok) {
+        const uint32_t drain_bar = ptx::smem_addr(&ctl.mma_drain);
+        ptx::tc_commit(drain_bar);
+        W.drain(drain_bar, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;           // epilogue warp 0..3
+    const int sub = warp & 3;          // tensor-memory sub-partition this warp may read
+    const int row = sub * 32 + lane;   // tile row owned by this thread
+    const uint32_t gather_bar = ptx::smem_addr(&ctl.epi_gather);
+    const uint32_t bcast_bar = ptx::smem_addr(&ctl.epi_bcast);
+    int ab = 0;
+    uint32_t aphase = 0;
+    uint32_t gphase = 0;
+    int buf = 0;
+    // Convert 64 fp32 columns of this thread's row to fp16, stage them as one
+    // 128-byte swizzled row of a 32 x 64 box and let lane 0 store the box.
+    auto store_chunk = [&](const Unit& x, int q, const float* v) {
+      const uint32_t sbuf = epi_base + (ew * 2 + buf) * Cfg::kEpiBufBytes;
+      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this buffer is done
+      __syncwarp();
+      const uint32_t row_addr = sbuf + lane * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float* f = v + 8 * j;
+        st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
+                     pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(&p.tmC[x.g], sbuf, x.tn * BN + 64 * q, x.tm * kBM + sub * 32, x.l);
+        ptx::bulk_commit();
+      }
+      buf ^= 1;
+    };
+    // Tensor memory -> registers, 64 columns of this thread's row.
+    auto load_chunk = [&](uint32_t t_addr, float* v) {
+      uint32_t r[64];
+      ptx::tmem_load_32cols(t_addr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      ptx::tmem_load_32cols(t_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      ptx::tmem_load_wait();
+      ptx::reg_fence32(&r[0]);
+      ptx::reg_fence32(&r[32]);
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+    };
+
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+      const Unit x = decode_unit(p, u);
+      if (!warp_wait(W, acc_full_bar(ab), aphase, kStatusTimeoutEpilogue)) break;
+      ptx::tc_fence_after_sync();
+      const uint32_t t_row = tmem + (static_cast<uint32_t>(sub * 32) << 16) + ab * BN;
+      const bool rows_live = x.tm * kBM + sub * 32 < p.M[x.g];  // else the whole box is past M
+      const int my_ab = ab;
+      if (++ab == Cfg::kAccBufs) {
+        ab = 0;
+        aphase ^= 1u;
+      }
+      auto release_acc = [&]() {
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(acc_empty_bar(my_ab));
+      };
+
+      if (x.splits == 1) {
+#pragma unroll 1
+        for (int q = 0; q < BN / 64; ++q) {
+          float v[64];
+          load_chunk(t_row + 64 * q, v);
+          if (q == BN / 64 - 1) release_acc();
+          if (rows_live) store_chunk(x, q, v);
+        }
+        continue;
+      }
+
+      // Split-K: publish this split's partial tile, column-major so that a
+      // warp's stores of one column are 128 contiguous bytes.
+      float* ws = p.workspace + static_cast<size_t>(u) * (BN * kBM) + row;
+#pragma unroll 1
+      for (int q = 0; q < BN / 64; ++q) {
+        float v[64];
+        load_chunk(t_row + 64 * q, v);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) __stcg(ws + (64 * q + c) * kBM, v[c]);
+      }
+      release_acc();
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(gather_bar);
+      bool ok = true;
+      if (ew == 0) {
+        ok = warp_wait(W, gather_bar, gphase, kStatusTimeoutEpilogue);
+        if (ok && lane == 0) {
+          __threadfence();
+          const int old = atomicAdd(&p.counters[x.tile], 1);
+          const int last = (old == x.splits - 1) ? 1 : 0;
+          if (last) __threadfence();
+          ctl.last_flag = last;
+          ptx::mbar_arrive(bcast_bar);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (!warp_wait(W, bcast_bar, gphase, kStatusTimeoutEpilogue)) break;
+      gphase ^= 1u;
+      if (!ctl.last_flag) continue;
+      __threadfence();
+      // Last arrival: sum the partials of splits 0..S-1 in that order, so the
+      // result does not depend on which split finished last.
+      const float* ws0 = p.workspace + static_cast<size_t>(u - x.split) * (BN * kBM) + row;
+#pragma unroll 1
+      for (int q = 0; q < BN / 64; ++q) {
+        float v[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) v[c] = 0.0f;
+        for (int j = 0; j < x.splits; ++j) {
+          const float* src = ws0 + static_cast<size_t>(j) * (BN * kBM) + (64 * q) * kBM;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) v[c] += __ldcg(src + c * kBM);
+        }
+        if (rows_live) store_chunk(x, q, v);
+      }
+      if (ew == 0 && lane == 0) p.counters[x.tile] = 0;  // ready for the next launch
+    }
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  if (warp == 1) ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+// ---------------------------------------------------------------- launcher
+template <int BN>
+static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
+  using Cfg = TileCfg<BN>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kDynSmem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN>, p);
+}
+
+template <int BN>
+static cudaError_t prepare_bn() {
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<BN>::kDynSmem);
+}
+
+cudaError_t gemm_prepare_device(int bn) {
+  switch (bn) {
+    case 128: return prepare_bn<128>();
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 128: return launch_bn<128>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int gemm_stages(int bn) {
+  switch (bn) {
+    case 128: return TileCfg<128>::kStages;
+    case 256: return TileCfg<256>::kStages;
+    default: return 0;
+  }
+}
+
+}  // namespace nvfp4

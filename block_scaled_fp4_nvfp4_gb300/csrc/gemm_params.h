@@ -1,0 +1,84 @@
+// Kernel parameter block and compile-time tiling shared by the host launcher
+// and the device kernel of libnvfp4gemm.  Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+constexpr int kMaxGroups = 8;
+
+// One CTA tile: 128 rows of A (the tcgen05 M=128 shape), BN rows of B, and
+// 256 K-elements per pipeline stage (128 bytes of packed E2M1 per row, i.e. one
+// 128-byte swizzle row).  "nvfp4 gemm, submission 125598" and
+// "nvfp4_group_gemm, submission 498453" use a 128x128x256 MMA tiler; that is
+// kept as the base tile here.
+constexpr int kBM = 128;
+constexpr int kBK = 256;
+constexpr int kBKBytes = kBK / 2;          // 128 B per row per k-tile
+constexpr int kMmaK = 64;                  // K of one kind::mxf4nvf4 MMA
+constexpr int kSfAtomBytes = 512;          // 128 rows x 4 scales
+constexpr int kSfSlabBytes = 4 * kSfAtomBytes;  // one 128-row block, one k-tile
+
+constexpr int kNumThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+
+// Status codes a kernel may leave in the device status word.
+constexpr int kStatusTimeoutProducer = 1;
+constexpr int kStatusTimeoutMma = 2;
+constexpr int kStatusTimeoutEpilogue = 3;
+
+// Host-built parameter block, passed by value as a __grid_constant__ kernel
+// parameter: the tensor maps live in the parameter space and need no device
+// allocation or copy (the pages keep them in a device blob instead).
+struct GemmParams {
+  CUtensorMap tmA[kMaxGroups];   // uint8 {K/2, M, L}, box {128, 128, 1}, 128B swizzle
+  CUtensorMap tmB[kMaxGroups];   // uint8 {K/2, N, L}, box {128, BN, 1}, 128B swizzle
+  CUtensorMap tmC[kMaxGroups];   // fp16 {N, M, L}, box {64, 32, 1}, 128B swizzle
+  const uint8_t* sfa[kMaxGroups];  // repacked scales
+  const uint8_t* sfb[kMaxGroups];
+  int M[kMaxGroups], N[kMaxGroups], L[kMaxGroups];
+  int ktiles[kMaxGroups];        // K / 256
+  int tiles_m[kMaxGroups], tiles_n[kMaxGroups];
+  int splits[kMaxGroups];        // split-K factor (1 = whole K per unit)
+  int sf_rows_a[kMaxGroups];     // ceil(M/128): 128-row scale blocks per batch
+  int sf_rows_b[kMaxGroups];     // ceil(N/128)
+  int a_streams[kMaxGroups];     // 1: A is the streamed operand (evict-first), B kept
+  int unit_start[kMaxGroups + 1];  // prefix over groups of work units
+  int tile_start[kMaxGroups + 1];  // prefix over groups of output tiles
+  int num_groups;
+  int total_units;
+  float* workspace;              // split-K partials, [unit][BN][128] fp32
+  int* counters;                 // per output tile arrival counters (zero between launches)
+  int* status;                   // device status word
+  unsigned long long timeout_ns; // limit of every bounded wait
+  int debug_skip_ktile;          // test-only fault injection (-1 = off)
+};
+
+// Per-BN compile-time configuration.
+template <int BN>
+struct TileCfg {
+  static constexpr int kBN = BN;
+  static constexpr int kABytes = kBM * kBKBytes;               // 16 KB
+  static constexpr int kBBytes = BN * kBKBytes;                // BN * 128 B
+  static constexpr int kSfbBlocks = (BN + 127) / 128;          // 128-row scale blocks
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfSlabBytes + kSfbBlocks * kSfSlabBytes;
+  static constexpr int kEpiBufBytes = 32 * 128;                // 32 rows x 64 fp16
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kSmemBudget = 227 * 1024;
+  static constexpr int kStages = (kSmemBudget - kEpiBytes - 1024) / kStageBytes;
+  static constexpr int kDynSmem = kStages * kStageBytes + kEpiBytes + 1024;  // +1024 alignment slack
+  // Tensor memory: accumulators first, then a ring of scale slots.
+  static constexpr int kAccBufs = (BN <= 128) ? 2 : 1;
+  static constexpr int kSfaCols = 4 * (kBK / kMmaK);               // 16 per k-tile
+  static constexpr int kSfbCols = (BN / 32) * (kBK / kMmaK);       // BN/32 per MMA
+  static constexpr int kSfSlots = 4;
+  static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
+  static constexpr int kSfBaseCol = kAccBufs * BN;
+  static constexpr int kTmemCols = 512;
+  static_assert(kSfBaseCol + kSfSlots * kSfSlotCols <= kTmemCols, "tensor memory overflow");
+  static_assert(kStages >= 2, "not enough shared memory for two stages");
+};
+
+}  // namespace nvfp4

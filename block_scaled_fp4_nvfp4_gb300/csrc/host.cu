@@ -1,0 +1,474 @@
+// C ABI of libnvfp4gemm: argument checks, launch planning, tensor-map
+// encoding and caching, per-stream split-K workspaces, the device status word.
+//
+// The host path of "nvfp4 group gemm, submission 407526" (group_gemm) checks
+// the group count, caches encoded tensor maps by pointer and shape, builds a
+// per-tile list and copies a descriptor blob to the device on every call.  Here
+// the tensor maps and the per-group metadata travel in the kernel's parameter
+// block instead (no device blob, no host->device copy per call), and the
+// persistent kernel derives its tiles from per-group prefix sums.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/nvfp4_gemm.h"
+#include "descriptors.h"
+#include "gemm_params.h"
+
+namespace nvfp4 {
+cudaError_t gemm_prepare_device(int bn);
+cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+int gemm_stages(int bn);
+cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return NVFP4_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(NVFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_debug_skip{-1};
+
+// ------------------------------------------------------------------ devices
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;       // device status word
+  bool prepared_bn128 = false;
+};
+
+struct Workspace {
+  float* partials = nullptr;
+  size_t partial_bytes = 0;
+  int* counters = nullptr;
+  size_t counter_count = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+int device_state(int dev, DeviceState** out) {
+  DeviceState& d = g_devices[dev];
+  if (!d.ready) {
+    cudaError_t e;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    if (d.cc_major != 10 || d.cc_minor != 3)
+      return fail(NVFP4_ERR_UNSUPPORTED_DEVICE,
+                  "device %d has compute capability %d.%d; this library is built for sm_103a only",
+                  dev, d.cc_major, d.cc_minor);
+    if ((e = cudaMalloc(&d.status, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+    if ((e = cudaMemset(d.status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    d.ready = true;
+  }
+  *out = &d;
+  return NVFP4_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  int kind;  // 0 operand, 1 C
+  uintptr_t ptr;
+  int rows, cols, L, box_rows;
+  bool operator==(const MapKey& o) const {
+    return kind == o.kind && ptr == o.ptr && rows == o.rows && cols == o.cols && L == o.L &&
+           box_rows == o.box_rows;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<uintptr_t>()(k.ptr);
+    h ^= (static_cast<size_t>(k.rows) * 0x9E3779B97F4A7C15ull) + (h << 6) + (h >> 2);
+    h ^= (static_cast<size_t>(k.cols) * 0xC2B2AE3D27D4EB4Full) + (h << 6) + (h >> 2);
+    h ^= static_cast<size_t>(k.L * 131 + k.box_rows * 7 + k.kind);
+    return h;
+  }
+};
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// K-major packed E2M1 operand [L][rows][K/2] bytes; box: 128 bytes x box_rows.
+int encode_operand_map(CUtensorMap* out, const void* ptr, int rows, int K, int L, int box_rows) {
+  MapKey key{0, reinterpret_cast<uintptr_t>(ptr), rows, K, L, box_rows};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return NVFP4_OK;
+  }
+  auto fn = encode_fn();
+  if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(K) / 2;
+  cuuint64_t dims[3] = {row_bytes, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(L)};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBKBytes), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled(operand rows=%d K=%d L=%d) failed: %d", rows, K,
+                L, static_cast<int>(r));
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return NVFP4_OK;
+}
+
+// fp16 C [L][M][N]; box: 64 columns x 32 rows.
+int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
+  MapKey key{1, reinterpret_cast<uintptr_t>(ptr), M, N, L, 32};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return NVFP4_OK;
+  }
+  auto fn = encode_fn();
+  if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(L)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N) * 2 * M};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled(C M=%d N=%d L=%d) failed: %d", M, N, L,
+                static_cast<int>(r));
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return NVFP4_OK;
+}
+
+// ------------------------------------------------------------------ planning
+struct Plan {
+  int bn = 128;
+  int stages = 0;
+  int total_units = 0;
+  int total_tiles = 0;
+  int grid = 0;
+  int splits[kMaxGroups] = {};
+  int tiles_m[kMaxGroups] = {}, tiles_n[kMaxGroups] = {};
+  int unit_start[kMaxGroups + 1] = {};
+  int tile_start[kMaxGroups + 1] = {};
+};
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+// Split-K only when the output tiles do not fill the machine: choose the
+// smallest S whose unit count packs into whole waves almost as well as the best
+// S, and keep at least 4 k-tiles per unit.
+int choose_split(long long tiles, const int* ktiles, int G, int sms) {
+  if (tiles >= sms) return 1;
+  int min_kt = ktiles[0];
+  for (int g = 1; g < G; ++g) min_kt = ktiles[g] < min_kt ? ktiles[g] : min_kt;
+  const int max_s = min_kt / 4 < 1 ? 1 : (min_kt / 4 > 32 ? 32 : min_kt / 4);
+  double eff[33] = {};
+  double best = 0.0;
+  for (int s = 1; s <= max_s; ++s) {
+    const long long u = tiles * s;
+    eff[s] = static_cast<double>(u) / static_cast<double>(cdiv(u, sms) * sms);
+    if (eff[s] > best) best = eff[s];
+  }
+  for (int s = 1; s <= max_s; ++s)
+    if (eff[s] >= best - 0.02) return s;
+  return 1;
+}
+
+int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl) {
+  pl->bn = 128;
+  pl->stages = gemm_stages(pl->bn);
+  int ktiles[kMaxGroups];
+  long long tiles = 0;
+  for (int g = 0; g < G; ++g) {
+    ktiles[g] = K[g] / kBK;
+    pl->tiles_m[g] = static_cast<int>(cdiv(M[g], kBM));
+    pl->tiles_n[g] = static_cast<int>(cdiv(N[g], pl->bn));
+    tiles += static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
+  }
+  const int s = choose_split(tiles, ktiles, G, sms);
+  long long units = 0, tcount = 0;
+  for (int g = 0; g < G; ++g) {
+    const long long tg = static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
+    int sg = s;
+    const int cap = ktiles[g] / 4 < 1 ? 1 : ktiles[g] / 4;
+    if (sg > cap) sg = cap;
+    pl->splits[g] = sg;
+    pl->unit_start[g] = static_cast<int>(units);
+    pl->tile_start[g] = static_cast<int>(tcount);
+    units += tg * sg;
+    tcount += tg;
+    if (units > 0x7FFFFFFFLL || tcount > 0x7FFFFFFFLL)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "problem has too many output tiles");
+  }
+  pl->unit_start[G] = static_cast<int>(units);
+  pl->tile_start[G] = static_cast<int>(tcount);
+  pl->total_units = static_cast<int>(units);
+  pl->total_tiles = static_cast<int>(tcount);
+  pl->grid = static_cast<int>(units < sms ? units : sms);
+  if (pl->grid < 1) pl->grid = 1;
+  return NVFP4_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shapes(int G, const int* M, const int* N, const int* K, const int* L) {
+  if (G < 1 || G > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_INVALID_ARG, "G=%d outside 1..%d", G, NVFP4_MAX_GROUPS);
+  if (!M || !N || !K || !L) return fail(NVFP4_ERR_INVALID_ARG, "null size array");
+  for (int g = 0; g < G; ++g) {
+    if (M[g] < 1 || N[g] < 1 || K[g] < 1 || L[g] < 1)
+      return fail(NVFP4_ERR_INVALID_ARG, "group %d: sizes must be >= 1 (M=%d N=%d K=%d L=%d)", g, M[g],
+                  N[g], K[g], L[g]);
+    if (K[g] % kBK != 0)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: K=%d is not a multiple of %d", g, K[g], kBK);
+    if (N[g] % 8 != 0)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: N=%d is not a multiple of 8", g, N[g]);
+    // tensor-map limits: every dimension < 2^32, byte strides < 2^40
+    const unsigned long long a_bytes = static_cast<unsigned long long>(M[g]) * (K[g] / 2);
+    const unsigned long long b_bytes = static_cast<unsigned long long>(N[g]) * (K[g] / 2);
+    const unsigned long long c_bytes = static_cast<unsigned long long>(M[g]) * N[g] * 2;
+    if (a_bytes >= (1ull << 40) || b_bytes >= (1ull << 40) || c_bytes >= (1ull << 40))
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: a matrix exceeds 2^40 bytes", g);
+  }
+  return NVFP4_OK;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t counters,
+                  Workspace** out) {
+  Workspace& w = g_workspaces[{dev, stream}];
+  cudaError_t e;
+  const bool grow = partial_bytes > w.partial_bytes || counters > w.counter_count;
+  if (grow) {
+    // the old buffers may still be in use by work queued on this stream
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    cudaFree(w.partials);
+    cudaFree(w.counters);
+    w = Workspace{};
+    const size_t pb = partial_bytes > 0 ? partial_bytes : 16;
+    const size_t cb = (counters > 0 ? counters : 1) * sizeof(int);
+    if ((e = cudaMalloc(&w.partials, pb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K workspace)");
+    if ((e = cudaMalloc(&w.counters, cb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K counters)");
+    if ((e = cudaMemsetAsync(w.counters, 0, cb, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    w.partial_bytes = pb;
+    w.counter_count = cb / sizeof(int);
+  }
+  *out = &w;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+size_t nvfp4_gemm_repacked_scales_bytes(int rows, int K, int L) {
+  if (rows < 1 || K < 1 || L < 1 || K % 16 != 0) return 0;
+  return static_cast<size_t>(L) * static_cast<size_t>(cdiv(rows, 128)) *
+         static_cast<size_t>(cdiv(K, 256) * 4) * kSfAtomBytes;
+}
+
+int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int K, int L, void* stream) {
+  if (!sf || !out) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(sf) || !aligned16(out)) return fail(NVFP4_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (rows < 1 || K < 16 || L < 1 || K % 16 != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "bad sizes rows=%d K=%d L=%d (K %% 16 == 0 required)", rows, K, L);
+  cudaError_t e = repack_launch(sf, out, rows, K, L, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+  return ok();
+}
+
+int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, const void* const* SFA,
+                           const void* const* SFB, void* const* C, const int* M, const int* N,
+                           const int* K, const int* L, void* stream_) {
+  int rc = check_shapes(G, M, N, K, L);
+  if (rc != NVFP4_OK) return rc;
+  if (!A || !B || !SFA || !SFB || !C) return fail(NVFP4_ERR_INVALID_ARG, "null pointer array");
+  for (int g = 0; g < G; ++g) {
+    if (!A[g] || !B[g] || !SFA[g] || !SFB[g] || !C[g])
+      return fail(NVFP4_ERR_INVALID_ARG, "group %d: null device pointer", g);
+    if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(SFA[g]) || !aligned16(SFB[g]) || !aligned16(C[g]))
+      return fail(NVFP4_ERR_INVALID_ARG, "group %d: device pointers must be 16-byte aligned", g);
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(dev, &ds)) != NVFP4_OK) return rc;
+
+  Plan pl;
+  if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
+  if (pl.bn == 128 && !ds->prepared_bn128) {
+    if ((e = gemm_prepare_device(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    ds->prepared_bn128 = true;
+  }
+
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  for (int g = 0; g < G; ++g) {
+    if ((rc = encode_operand_map(&p.tmA[g], A[g], M[g], K[g], L[g], kBM)) != NVFP4_OK) return rc;
+    if ((rc = encode_operand_map(&p.tmB[g], B[g], N[g], K[g], L[g], pl.bn)) != NVFP4_OK) return rc;
+    if ((rc = encode_c_map(&p.tmC[g], C[g], M[g], N[g], L[g])) != NVFP4_OK) return rc;
+    p.sfa[g] = static_cast<const uint8_t*>(SFA[g]);
+    p.sfb[g] = static_cast<const uint8_t*>(SFB[g]);
+    p.M[g] = M[g];
+    p.N[g] = N[g];
+    p.L[g] = L[g];
+    p.ktiles[g] = K[g] / kBK;
+    p.tiles_m[g] = pl.tiles_m[g];
+    p.tiles_n[g] = pl.tiles_n[g];
+    p.splits[g] = pl.splits[g];
+    p.sf_rows_a[g] = static_cast<int>(cdiv(M[g], 128));
+    p.sf_rows_b[g] = static_cast<int>(cdiv(N[g], 128));
+    // The larger operand streams through L2 once (evict-first); the smaller,
+    // re-read by every tile along the other dimension, is kept (evict-last).
+    // Same rule as "nvfp4 group gemm, submission 407526" (cache_A / cache_B).
+    p.a_streams[g] = M[g] > N[g] ? 1 : 0;
+  }
+  for (int g = 0; g <= G; ++g) {
+    p.unit_start[g] = pl.unit_start[g];
+    p.tile_start[g] = pl.tile_start[g];
+  }
+  p.num_groups = G;
+  p.total_units = pl.total_units;
+  p.status = ds->status;
+  p.timeout_ns = g_timeout_ns.load();
+  p.debug_skip_ktile = g_debug_skip.exchange(-1);
+
+  bool any_split = false;
+  for (int g = 0; g < G; ++g) any_split |= pl.splits[g] > 1;
+  if (any_split) {
+    Workspace* w = nullptr;
+    const size_t partial_bytes = static_cast<size_t>(pl.total_units) * kBM * pl.bn * sizeof(float);
+    if ((rc = get_workspace(dev, stream, partial_bytes, pl.total_tiles, &w)) != NVFP4_OK) return rc;
+    p.workspace = w->partials;
+    p.counters = w->counters;
+  }
+
+  e = gemm_launch(pl.bn, p, pl.grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  return ok();
+}
+
+int nvfp4_gemm_run(const void* A, const void* B, const void* SFA, const void* SFB, void* C, int M, int N,
+                   int K, int L, void* stream) {
+  const void* a[1] = {A};
+  const void* b[1] = {B};
+  const void* sa[1] = {SFA};
+  const void* sb[1] = {SFB};
+  void* c[1] = {C};
+  return nvfp4_gemm_run_grouped(1, a, b, sa, sb, c, &M, &N, &K, &L, stream);
+}
+
+const char* nvfp4_gemm_last_error_string(void) { return g_last_error.c_str(); }
+
+int nvfp4_gemm_check_device_status(void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  int rc = device_state(dev, &ds);
+  if (rc != NVFP4_OK) return rc;
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int h = 0;
+  if ((e = cudaMemcpy(&h, ds->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(status)");
+  if (h != 0) {
+    // An aborted launch may leave split-K arrival counters non-zero: clear
+    // every workspace of this device before reporting.
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    if ((e = cudaMemset(ds->status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    for (auto& kv : g_workspaces)
+      if (kv.first.first == dev && kv.second.counters)
+        if ((e = cudaMemset(kv.second.counters, 0, kv.second.counter_count * sizeof(int))) != cudaSuccess)
+          return cuda_fail(e, "cudaMemset(counters)");
+    return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a bounded wait ran out on the device (role code %d)", h);
+  }
+  return ok();
+}
+
+int nvfp4_gemm_set_wait_timeout_ns(uint64_t ns) {
+  if (ns < 100000ull) return fail(NVFP4_ERR_INVALID_ARG, "timeout below 1e5 ns");
+  g_timeout_ns.store(ns);
+  return ok();
+}
+
+int nvfp4_gemm_debug_inject_skip(int ktile) {
+  g_debug_skip.store(ktile < 0 ? -1 : ktile);
+  return ok();
+}
+
+int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L, int num_sms, int* out,
+                    int out_len) {
+  int rc = check_shapes(G, M, N, K, L);
+  if (rc != NVFP4_OK) return rc;
+  if (num_sms < 1 || !out || out_len < 4 + G) return fail(NVFP4_ERR_INVALID_ARG, "bad plan arguments");
+  Plan pl;
+  if ((rc = make_plan(G, M, N, K, L, num_sms, &pl)) != NVFP4_OK) return rc;
+  out[0] = pl.bn;
+  out[1] = pl.total_units;
+  out[2] = pl.grid;
+  out[3] = pl.stages;
+  for (int g = 0; g < G; ++g) out[4 + g] = pl.splits[g];
+  return ok();
+}
+
+uint32_t nvfp4_gemm_encode_idesc(int M, int N) { return make_idesc_nvf4(M, N); }
+
+uint64_t nvfp4_gemm_encode_smem_desc(uint32_t smem_addr, int swizzle128) {
+  return swizzle128 ? operand_desc(smem_addr) : scale_desc(smem_addr);
+}
+
+}  // extern "C"

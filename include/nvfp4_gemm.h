@@ -1,0 +1,169 @@
+/*
+ * nvfp4_gemm.h -- C ABI of libnvfp4gemm.so, a GB300 (sm_103a) NVFP4
+ * block-scaled GEMM, dense and grouped.
+ *
+ * The operation (stated alike on all three source pages: "nvfp4_group_gemm,
+ * submission 498453", custom_kernel docstring "C = A * SFA * B * SFB for all
+ * groups", and the MMA-loop comment of that page and of "nvfp4 gemm,
+ * submission 125598"):
+ *
+ *   C[l][m][n] = fp16( sum_k e2m1(A[l][m][k]) * e4m3(SFA[l][m][k/16])
+ *                           * e2m1(B[l][n][k]) * e4m3(SFB[l][n][k/16]) )
+ *
+ * accumulated in fp32 by the tensor cores and rounded to fp16 (RNE) once.
+ *
+ * Layouts (device memory, row-major, l outermost):
+ *   A    [L][M][K/2]  uint8, two E2M1 codes per byte, element 2i in the low
+ *                     nibble of byte i (float4_e2m1fn_x2), K-major;
+ *   B    [L][N][K/2]  same as A;
+ *   SFA, SFB          E4M3 (float8_e4m3fn) scales in the REPACKED layout
+ *                     produced by nvfp4_gemm_repack_scales (below);
+ *   C    [L][M][N]    fp16.
+ *
+ * Conventions for every entry point:
+ *   - All pointers named "device" are device pointers on the current CUDA
+ *     device; the caller owns them and keeps them alive until the work queued
+ *     on `stream` has finished.  Host arrays are read before the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  All work is asynchronous on that stream; nothing synchronises
+ *     unless stated.
+ *   - Return value: NVFP4_OK or a negative nvfp4_status.  On error nothing is
+ *     queued, and nvfp4_gemm_last_error_string() (per calling thread) says why.
+ *     The library never aborts the process.
+ *   - Every device buffer must be 16-byte aligned.
+ */
+#ifndef NVFP4_GEMM_H
+#define NVFP4_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = -1,       /* null / misaligned pointer, size < 1, G outside 1..8 */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = -2, /* K % 256 != 0, N % 8 != 0, size beyond limits */
+    NVFP4_ERR_CUDA = -3,              /* a CUDA runtime / driver call failed */
+    NVFP4_ERR_DEVICE_TIMEOUT = -4,    /* a kernel's bounded wait ran out (see below) */
+    NVFP4_ERR_UNSUPPORTED_DEVICE = -5 /* the current device is not sm_103 */
+} nvfp4_status;
+
+/* Largest number of problems one grouped call takes ("expected 1..8 groups",
+ * "nvfp4 group gemm, submission 407526", group_gemm argument checks). */
+#define NVFP4_MAX_GROUPS 8
+
+/*
+ * Size in bytes of the repacked scale buffer for a [L][rows][K/16] scale
+ * tensor: L * ceil(rows/128) * (4*ceil(K/256)) * 512.
+ * Returns 0 for rows < 1, K < 1, L < 1 or K % 16 != 0.
+ */
+NVFP4_API size_t nvfp4_gemm_repacked_scales_bytes(int rows, int K, int L);
+
+/*
+ * Repack row-major E4M3 scales into the tensor-core scale layout.
+ *
+ * Layout ("nvfp4 gemm, submission 125598", custom_kernel docstring: permuted
+ * scales of logical shape [32, 4, rest_m, 4, rest_k, l]; "nvfp4 group gemm,
+ * submission 407526", grouped_kernel TMA producer: one 512-byte atom per
+ * (128-row block, 4 scale columns), 2048 bytes per 256-wide k-tile):
+ *   out[l][rm][ck][r0][r1][c0] = sf[l][128*rm + 32*r1 + r0][4*ck + c0]
+ * with r0 < 32, r1 < 4, c0 < 4, rm < ceil(rows/128), ck < 4*ceil(K/256);
+ * positions outside the input are zero.
+ *
+ *   sf     device, [L][rows][K/16] bytes, row-major, 16-byte aligned
+ *   out    device, nvfp4_gemm_repacked_scales_bytes(rows, K, L) bytes
+ *   rows   M for SFA, N for SFB (>= 1);  K >= 16, K % 16 == 0;  L >= 1
+ * Errors: INVALID_ARG (null/misaligned pointer, sizes), CUDA.
+ */
+NVFP4_API int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int K, int L, void* stream);
+
+/*
+ * One problem: C = A * SFA * B * SFB ("nvfp4 gemm, submission 125598",
+ * custom_kernel).  Equivalent to nvfp4_gemm_run_grouped with G = 1.
+ *
+ *   A    device [L][M][K/2]       SFA  device, repacked (rows = M)
+ *   B    device [L][N][K/2]       SFB  device, repacked (rows = N)
+ *   C    device [L][M][N] fp16, written (rows >= M and columns >= N untouched)
+ * Shape contract: M, N, K, L >= 1; K % 256 == 0; N % 8 == 0 (16-byte C rows).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, UNSUPPORTED_DEVICE, CUDA.
+ */
+NVFP4_API int nvfp4_gemm_run(const void* A, const void* B, const void* SFA, const void* SFB, void* C,
+                   int M, int N, int K, int L, void* stream);
+
+/*
+ * G independent problems in one launch ("nvfp4 group gemm, submission
+ * 407526", group_gemm; "nvfp4_group_gemm, submission 498453", custom_kernel:
+ * "each group has its own a, b, c, sfa, sfb with different m, n, k, l").
+ *
+ *   G                1..NVFP4_MAX_GROUPS
+ *   A, B, SFA, SFB, C  host arrays of G device pointers, per group as in
+ *                    nvfp4_gemm_run
+ *   M, N, K, L       host arrays of G sizes, per group as in nvfp4_gemm_run
+ * Errors: as nvfp4_gemm_run; the first offending group is named.
+ */
+NVFP4_API int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B,
+                           const void* const* SFA, const void* const* SFB, void* const* C,
+                           const int* M, const int* N, const int* K, const int* L, void* stream);
+
+/* Text of the last error on the calling thread ("" if none).  The pointer
+ * stays valid until the next call from the same thread. */
+NVFP4_API const char* nvfp4_gemm_last_error_string(void);
+
+/*
+ * Device-side failure detection.  Every wait inside the kernels is bounded:
+ * when one runs out, the kernel records NVFP4_ERR_DEVICE_TIMEOUT in a status
+ * word on the device, stops issuing work, waits for its own copies in flight,
+ * frees its tensor memory and returns.  Its output is then undefined.
+ *
+ * nvfp4_gemm_check_device_status synchronises `stream`, reads and clears the
+ * current device's status word and returns NVFP4_OK or
+ * NVFP4_ERR_DEVICE_TIMEOUT (or CUDA if the synchronisation itself failed).
+ */
+NVFP4_API int nvfp4_gemm_check_device_status(void* stream);
+
+/* Limit of every bounded wait, in nanoseconds (default 2e9; minimum 1e5).
+ * Applies to launches made after the call, on all devices. */
+NVFP4_API int nvfp4_gemm_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Fault injection for tests: when `ktile` >= 0, CTA 0's producer skips the
+ * arrival for its ktile-th k-tile of the next launch only, so that a consumer
+ * wait runs out.  Nothing is copied for that k-tile, so no copy is left in
+ * flight.  -1 disables.  Not for production use.
+ */
+NVFP4_API int nvfp4_gemm_debug_inject_skip(int ktile);
+
+/*
+ * Launch plan, host only (no GPU needed): what nvfp4_gemm_run_grouped would
+ * launch for these sizes on a device with `num_sms` SMs.
+ *   out[0] tile width BN along N       out[1] total work units
+ *   out[2] grid size (CTAs)            out[3] pipeline stages
+ *   out[4 + g] split-K factor of group g (g < G)
+ */
+NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L,
+                    int num_sms, int* out, int out_len);
+
+/*
+ * Descriptor encoders used by the kernel, exported for host-side checks.
+ *   nvfp4_gemm_encode_idesc: tcgen05.mma kind::mxf4nvf4 instruction
+ *     descriptor for E2M1 x E2M1 with E4M3 block-16 scales, K-major operands.
+ *   nvfp4_gemm_encode_smem_desc: shared-memory matrix descriptor;
+ *     swizzle128 = 1 for the K-major 128-byte-swizzled operand tiles
+ *     (8-row stride 1024 B), 0 for the unswizzled scale atoms (stride 128 B).
+ */
+NVFP4_API uint32_t nvfp4_gemm_encode_idesc(int M, int N);
+NVFP4_API uint64_t nvfp4_gemm_encode_smem_desc(uint32_t smem_addr, int swizzle128);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_GEMM_H */

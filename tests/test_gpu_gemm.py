@@ -1,0 +1,144 @@
+"""GPU GEMM parity against the CPU oracle, through the C ABI.
+
+Tolerance (elementwise): |gpu - ref| <= 1e-3 * sum_k |a_k b_k| + 1 ulp_fp16(ref).
+Small problems are compared whole; the five workloads at full size are
+compared on sampled outputs (random points plus every tile's corners).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_fp4_nvfp4_gb300 import workloads
+from gpu_util import (alloc_c, assert_close_full, assert_close_points, check_canary, require_gpu,
+                      run_single, sample_points, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def test_single_tile_workload():
+    binding = require_gpu()
+    p = workloads.make_inputs("single_128x128x256", seed=0)[0]
+    d = to_device(p)
+    buf, C = alloc_c(128, 128, 1)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, 128, 128, 1)
+
+
+@pytest.mark.parametrize("M,N,K,L", [
+    (128, 128, 512, 1),
+    (256, 256, 1024, 1),
+    (1, 8, 256, 1),          # smallest legal problem
+    (64, 128, 256, 1),       # half an M tile
+    (192, 128, 768, 1),      # ragged M tile
+    (200, 136, 512, 1),      # ragged M and N tiles
+    (129, 264, 256, 2),      # batches, ragged everywhere
+    (384, 384, 2048, 1),     # several tiles, deeper K than the stage ring
+    (128, 1024, 8192, 1),    # skinny: split-K path
+    (64, 2048, 4096, 1),     # skinny, partial M tile, split-K
+])
+def test_parity_small(M, N, K, L):
+    binding = require_gpu()
+    p = workloads.make_random_problem(M * 7 + N * 3 + K + L, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
+
+
+def test_one_hot_scales_pin_the_atom_layout():
+    """Unit scales except one (row, k-block) per operand: a misplaced scale
+    byte changes exactly the rows/columns it lands in."""
+    binding = require_gpu()
+    M, N, K = 256, 256, 512
+    rng = np.random.default_rng(3)
+    for trial in range(4):
+        p = workloads.make_random_problem(50 + trial, M, N, K)
+        p["SFA"].fill_(0x38)
+        p["SFB"].fill_(0x38)
+        ra, ca = int(rng.integers(0, M)), int(rng.integers(0, K // 16))
+        rb, cb = int(rng.integers(0, N)), int(rng.integers(0, K // 16))
+        p["SFA"][0, ra, ca] = 0x50   # 16.0
+        p["SFB"][0, rb, cb] = 0x28   # 0.25
+        d = to_device(p)
+        _, C = alloc_c(M, N, 1)
+        run_single(d, C)
+        binding.nvfp4_gemm_check_device_status()
+        assert_close_full(C, p)
+
+
+def test_split_k_is_deterministic():
+    binding = require_gpu()
+    p = workloads.make_random_problem(11, 128, 2048, 8192)
+    plan = binding.nvfp4_gemm_plan([128], [2048], [8192], [1], torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["splits"][0] > 1
+    d = to_device(p)
+    outs = []
+    for _ in range(3):
+        _, C = alloc_c(128, 2048, 1)
+        run_single(d, C)
+        torch.cuda.synchronize()
+        outs.append(C.clone())
+    binding.nvfp4_gemm_check_device_status()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))
+    assert_close_full(outs[0], p)
+
+
+def test_grouped_small_equals_oracle_and_singles():
+    binding = require_gpu()
+    shapes = [(128, 256, 512, 1), (64, 136, 256, 1), (300, 128, 1024, 2), (128, 1024, 4096, 1)]
+    probs = [workloads.make_random_problem(200 + i, *s) for i, s in enumerate(shapes)]
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    binding.nvfp4_gemm_run_grouped(
+        len(probs), [d["A"] for d in devs], [d["B"] for d in devs], [d["SFA"] for d in devs],
+        [d["SFB"] for d in devs], [c for _, c in Cs], [p["M"] for p in probs], [p["N"] for p in probs],
+        [p["K"] for p in probs], [p["L"] for p in probs])
+    binding.nvfp4_gemm_check_device_status()
+    refs = oracle.gemm_grouped(probs)
+    for p, d, (buf, c), ref in zip(probs, devs, Cs, refs):
+        check_canary(buf, p["M"], p["N"], p["L"])
+        assert_close_full(c, p)
+        # grouped launch == single launch of the same problem, bit for bit
+        _, c1 = alloc_c(p["M"], p["N"], p["L"])
+        run_single(d, c1)
+        torch.cuda.synchronize()
+        if binding.nvfp4_gemm_plan([p["M"]], [p["N"]], [p["K"]], [p["L"]], 152)["splits"] == [1]:
+            assert torch.equal(c.view(torch.int16), c1.view(torch.int16))
+
+
+def _run_workload(name):
+    binding = require_gpu()
+    probs = workloads.make_inputs(name, seed=0)
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    if len(probs) == 1:
+        run_single(devs[0], Cs[0][1])
+    else:
+        binding.nvfp4_gemm_run_grouped(
+            len(probs), [d["A"] for d in devs], [d["B"] for d in devs], [d["SFA"] for d in devs],
+            [d["SFB"] for d in devs], [c for _, c in Cs], [p["M"] for p in probs],
+            [p["N"] for p in probs], [p["K"] for p in probs], [p["L"] for p in probs])
+    binding.nvfp4_gemm_check_device_status()
+    return probs, Cs
+
+
+@pytest.mark.parametrize("name", ["skinny_128x7168x16384", "dense_8192x8192x8192", "grouped2", "moe8"])
+def test_workload_full_size_sampled(name):
+    probs, Cs = _run_workload(name)
+    for i, (p, (buf, C)) in enumerate(zip(probs, Cs)):
+        check_canary(buf, p["M"], p["N"], p["L"])
+        assert not torch.isnan(C).any(), "unwritten output elements"
+        ls, ms, ns = sample_points(p["M"], p["N"], p["L"], 1500, seed=i)
+        assert_close_points(C, p, ls, ms, ns)
+
+
+def test_skinny_workload_whole_output():
+    """The bench workload compared on every output element."""
+    probs, Cs = _run_workload("skinny_128x7168x16384")
+    assert_close_full(Cs[0][1], probs[0])
