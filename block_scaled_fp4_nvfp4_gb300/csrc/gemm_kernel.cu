@@ -41,7 +41,6 @@ constexpr int kMaxStages = 8;
 struct SmemCtl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t sf_free[8];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t epi_gather;
@@ -111,13 +110,12 @@ struct Waiter {
   }
 };
 
-// Lane 0 waits, the result is broadcast, the warp reconverges.
+// Every lane polls the barrier; the vote makes the outcome warp-uniform and
+// reconverges the warp (a lane that saw the phase complete just as another one
+// gave up still aborts with it).
 __device__ __forceinline__ bool warp_wait(const Waiter& W, uint32_t bar, uint32_t parity, int code) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = W.wait(bar, parity, code);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
+  const bool ok = W.wait(bar, parity, code);
+  return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -152,7 +150,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   auto full_bar = [&](int s) { return ptx::smem_addr(&ctl.full[s]); };
   auto empty_bar = [&](int s) { return ptx::smem_addr(&ctl.empty[s]); };
-  auto sf_free_bar = [&](int s) { return ptx::smem_addr(&ctl.sf_free[s]); };
   auto acc_full_bar = [&](int b) { return ptx::smem_addr(&ctl.acc_full[b]); };
   auto acc_empty_bar = [&](int b) { return ptx::smem_addr(&ctl.acc_empty[b]); };
 
@@ -161,7 +158,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
-    for (int s = 0; s < Cfg::kSfSlots; ++s) ptx::mbar_init(sf_free_bar(s), 1);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full_bar(b), 1);
       ptx::mbar_init(acc_empty_bar(b), kEpiWarps);
@@ -193,145 +189,142 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_stream = ptx::policy_evict_first();
-      const uint64_t pol_keep = ptx::policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      int armed[kStages];
+    // The whole warp runs the loop with warp-uniform values; one elected lane
+    // issues each copy (see the *_elect wrappers).
+    const uint64_t pol_stream = ptx::policy_evict_first();
+    const uint64_t pol_keep = ptx::policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed[kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) armed[s] = -1;
-      int count = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-        const Unit x = decode_unit(p, u);
-        const CUtensorMap* mapA = &p.tmA[x.g];
-        const CUtensorMap* mapB = &p.tmB[x.g];
-        const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
-        const uint64_t polB = p.a_streams[x.g] ? pol_keep : pol_stream;
-        const size_t atoms_per_block = static_cast<size_t>(p.ktiles[x.g]) * 4;
-        const uint8_t* sfa = p.sfa[x.g] +
-            (static_cast<size_t>(x.l) * p.sf_rows_a[x.g] + x.tm) * atoms_per_block * kSfAtomBytes;
-        const int sfb_block0 = x.tn * Cfg::kSfbBlocks;
-        const uint8_t* sfb = p.sfb[x.g] +
-            (static_cast<size_t>(x.l) * p.sf_rows_b[x.g] + sfb_block0) * atoms_per_block * kSfAtomBytes;
-        int nsfb = p.sf_rows_b[x.g] - sfb_block0;
-        nsfb = nsfb < Cfg::kSfbBlocks ? nsfb : Cfg::kSfbBlocks;
-        const uint32_t stage_tx =
-            Cfg::kABytes + Cfg::kBBytes + kSfSlabBytes + static_cast<uint32_t>(nsfb) * kSfSlabBytes;
-        for (int kt = x.kt0; kt < x.kt1; ++kt) {
-          if (!W.wait(empty_bar(stage), phase ^ 1u, kStatusTimeoutProducer)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
-          const uint32_t sB = sA + Cfg::kABytes;
-          const uint32_t sSFA = sB + Cfg::kBBytes;
-          const uint32_t sSFB = sSFA + kSfSlabBytes;
-          if (blockIdx.x == 0 && count == p.debug_skip_ktile) {
-            armed[stage] = -1;  // test-only: nothing issued, nothing in flight
-          } else {
-            const uint32_t fb = full_bar(stage);
-            ptx::mbar_arrive_expect_tx(fb, stage_tx);
-            ptx::tma_load_3d(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
-            ptx::tma_load_3d(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
-            ptx::bulk_load(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
-            for (int j = 0; j < nsfb; ++j)
-              ptx::bulk_load(sSFB + j * kSfSlabBytes,
-                             sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
-                             kSfSlabBytes, fb, polB);
-            armed[stage] = static_cast<int>(phase);
-          }
-          ++count;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+    for (int s = 0; s < kStages; ++s) armed[s] = -1;
+    int count = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+      const Unit x = decode_unit(p, u);
+      const CUtensorMap* mapA = &p.tmA[x.g];
+      const CUtensorMap* mapB = &p.tmB[x.g];
+      const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
+      const uint64_t polB = p.a_streams[x.g] ? pol_keep : pol_stream;
+      const size_t atoms_per_block = static_cast<size_t>(p.ktiles[x.g]) * 4;
+      const uint8_t* sfa = p.sfa[x.g] +
+          (static_cast<size_t>(x.l) * p.sf_rows_a[x.g] + x.tm) * atoms_per_block * kSfAtomBytes;
+      const int sfb_block0 = x.tn * Cfg::kSfbBlocks;
+      const uint8_t* sfb = p.sfb[x.g] +
+          (static_cast<size_t>(x.l) * p.sf_rows_b[x.g] + sfb_block0) * atoms_per_block * kSfAtomBytes;
+      int nsfb = p.sf_rows_b[x.g] - sfb_block0;
+      nsfb = nsfb < Cfg::kSfbBlocks ? nsfb : Cfg::kSfbBlocks;
+      const uint32_t stage_tx =
+          Cfg::kABytes + Cfg::kBBytes + kSfSlabBytes + static_cast<uint32_t>(nsfb) * kSfSlabBytes;
+      for (int kt = x.kt0; kt < x.kt1; ++kt) {
+        if (!warp_wait(W, empty_bar(stage), phase ^ 1u, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
+        const uint32_t sB = sA + Cfg::kABytes;
+        const uint32_t sSFA = sB + Cfg::kBBytes;
+        const uint32_t sSFB = sSFA + kSfSlabBytes;
+        if (blockIdx.x == 0 && count == p.debug_skip_ktile) {
+          armed[stage] = -1;  // test-only: nothing issued, nothing in flight
+        } else {
+          const uint32_t fb = full_bar(stage);
+          ptx::mbar_arrive_expect_tx_elect(fb, stage_tx);
+          ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
+          ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
+          ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
+          for (int j = 0; j < nsfb; ++j)
+            ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
+                                 sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
+                                 kSfSlabBytes, fb, polB);
+          armed[stage] = static_cast<int>(phase);
+        }
+        ++count;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok) {
-        // Shutting down: wait for the copies this thread put in flight.
+    }
+    if (!ok) {
+      // Shutting down: wait for the copies this warp put in flight.
+      if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
           if (armed[s] >= 0) W.drain(full_bar(s), static_cast<uint32_t>(armed[s]));
       }
+      __syncwarp();
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_nvf4(kBM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      int ab = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-        const Unit x = decode_unit(p, u);
-        if (!W.wait(acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
+    // Whole warp in the loop, one elected lane issues every tcgen05 operation
+    // (always the same lane, so its commits track all of them).
+    constexpr uint32_t idesc = make_idesc_nvf4(kBM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int ab = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+      const Unit x = decode_unit(p, u);
+      if (!warp_wait(W, acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after_sync();
+      const uint32_t d_tmem = tmem + ab * BN;
+      for (int kt = x.kt0; kt < x.kt1; ++kt) {
+        if (!warp_wait(W, full_bar(stage), phase, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
+        // Scale slot = smem stage: the stage was refilled only after the MMAs
+        // that last read this slot completed (they released the stage), so a
+        // completed "full" phase also means the slot is free to overwrite.
+        const int slot = stage;
         ptx::tc_fence_after_sync();
-        const uint32_t d_tmem = tmem + ab * BN;
-        for (int kt = x.kt0; kt < x.kt1; ++kt) {
-          if (!W.wait(full_bar(stage), phase, kStatusTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          const int slot = it % Cfg::kSfSlots;
-          const int use = it / Cfg::kSfSlots;
-          if (use > 0 && !W.wait(sf_free_bar(slot), static_cast<uint32_t>(use - 1) & 1u, kStatusTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after_sync();
-          const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
-          const uint32_t sB = sA + Cfg::kABytes;
-          const uint32_t sSFA = sB + Cfg::kBBytes;
-          const uint32_t sSFB = sSFA + kSfSlabBytes;
-          const uint32_t sfa_t = tmem + Cfg::kSfBaseCol + slot * Cfg::kSfSlotCols;
-          const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-          // Scale atoms -> tensor memory.  Atom kb of a 128-row block holds
-          // the 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
+        const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
+        const uint32_t sB = sA + Cfg::kABytes;
+        const uint32_t sSFA = sB + Cfg::kBBytes;
+        const uint32_t sSFB = sSFA + kSfSlabBytes;
+        const uint32_t sfa_t = tmem + Cfg::kSfBaseCol + slot * Cfg::kSfSlotCols;
+        const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+        // Scale atoms -> tensor memory.  Atom kb of a 128-row block holds the
+        // 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
 #pragma unroll
-          for (int kb = 0; kb < kBK / kMmaK; ++kb) {
-            ptx::tc_copy_sf(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+        for (int kb = 0; kb < kBK / kMmaK; ++kb) {
+          ptx::tc_copy_sf_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
 #pragma unroll
-            for (int j = 0; j < Cfg::kSfbBlocks; ++j)
-              ptx::tc_copy_sf(sfb_t + kb * (BN / 32) + 4 * j,
-                              scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes));
-          }
-#pragma unroll
-          for (int kb = 0; kb < kBK / kMmaK; ++kb) {
-            // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
-            ptx::tc_mma_nvf4(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
-                             sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
-                             (kt > x.kt0 || kb > 0) ? 1u : 0u);
-          }
-          ptx::tc_commit(empty_bar(stage));
-          ptx::tc_commit(sf_free_bar(slot));
-          ++it;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          for (int j = 0; j < Cfg::kSfbBlocks; ++j)
+            ptx::tc_copy_sf_elect(sfb_t + kb * (BN / 32) + 4 * j,
+                                  scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes));
         }
-        if (!ok) break;
-        ptx::tc_commit(acc_full_bar(ab));
-        if (++ab == Cfg::kAccBufs) {
-          ab = 0;
-          aphase ^= 1u;
+#pragma unroll
+        for (int kb = 0; kb < kBK / kMmaK; ++kb) {
+          // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
+          ptx::tc_mma_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
+                                 sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
+                                 (kt > x.kt0 || kb > 0) ? 1u : 0u);
+        }
+        ptx::tc_commit_elect(empty_bar(stage));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok) {
-        const uint32_t drain_bar = ptx::smem_addr(&ctl.mma_drain);
-        ptx::tc_commit(drain_bar);
-        W.drain(drain_bar, 0);
+      if (!ok) break;
+      ptx::tc_commit_elect(acc_full_bar(ab));
+      if (++ab == Cfg::kAccBufs) {
+        ab = 0;
+        aphase ^= 1u;
       }
     }
-    __syncwarp();
+    if (!ok) {
+      const uint32_t drain_bar = ptx::smem_addr(&ctl.mma_drain);
+      ptx::tc_commit_elect(drain_bar);
+      if (lane == 0) W.drain(drain_bar, 0);
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;           // epilogue warp 0..3

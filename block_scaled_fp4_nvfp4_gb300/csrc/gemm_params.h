@@ -73,7 +73,7 @@ struct TileCfg {
   static constexpr int kAccBufs = (BN <= 128) ? 2 : 1;
   static constexpr int kSfaCols = 4 * (kBK / kMmaK);               // 16 per k-tile
   static constexpr int kSfbCols = (BN / 32) * (kBK / kMmaK);       // BN/32 per MMA
-  static constexpr int kSfSlots = 4;
+  static constexpr int kSfSlots = kStages;  // one tensor-memory scale slot per smem stage
   static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
   static constexpr int kSfBaseCol = kAccBufs * BN;
   static constexpr int kTmemCols = 512;

@@ -14,6 +14,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -203,24 +204,19 @@ struct Plan {
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// Split-K only when the output tiles do not fill the machine: choose the
-// smallest S whose unit count packs into whole waves almost as well as the best
-// S, and keep at least 4 k-tiles per unit.
+// Split-K only when the output tiles do not fill the machine.  Measured on
+// GB300 (128 x 7168 x 16384): splits beyond one wave of units cost more in
+// partial-tile traffic and reduction than they gain in parallelism, so S is
+// the largest factor that keeps tiles * S within one wave, with at least 4
+// k-tiles per unit.
 int choose_split(long long tiles, const int* ktiles, int G, int sms) {
   if (tiles >= sms) return 1;
   int min_kt = ktiles[0];
   for (int g = 1; g < G; ++g) min_kt = ktiles[g] < min_kt ? ktiles[g] : min_kt;
   const int max_s = min_kt / 4 < 1 ? 1 : (min_kt / 4 > 32 ? 32 : min_kt / 4);
-  double eff[33] = {};
-  double best = 0.0;
-  for (int s = 1; s <= max_s; ++s) {
-    const long long u = tiles * s;
-    eff[s] = static_cast<double>(u) / static_cast<double>(cdiv(u, sms) * sms);
-    if (eff[s] > best) best = eff[s];
-  }
-  for (int s = 1; s <= max_s; ++s)
-    if (eff[s] >= best - 0.02) return s;
-  return 1;
+  long long s = sms / tiles;
+  if (s > max_s) s = max_s;
+  return s < 1 ? 1 : static_cast<int>(s);
 }
 
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl) {
@@ -234,13 +230,19 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     pl->tiles_n[g] = static_cast<int>(cdiv(N[g], pl->bn));
     tiles += static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
   }
-  const int s = choose_split(tiles, ktiles, G, sms);
+  int s = choose_split(tiles, ktiles, G, sms);
+  // Tuning / test override of the split-K factor (capped per group below).
+  if (const char* env = getenv("NVFP4_SPLIT_K")) {
+    const int v = atoi(env);
+    if (v >= 1 && v <= 64) s = v;
+  }
   long long units = 0, tcount = 0;
   for (int g = 0; g < G; ++g) {
     const long long tg = static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
     int sg = s;
     const int cap = ktiles[g] / 4 < 1 ? 1 : ktiles[g] / 4;
     if (sg > cap) sg = cap;
+    if (sg > ktiles[g]) sg = ktiles[g];
     pl->splits[g] = sg;
     pl->unit_start[g] = static_cast<int>(units);
     pl->tile_start[g] = static_cast<int>(tcount);
@@ -287,6 +289,12 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t cou
   cudaError_t e;
   const bool grow = partial_bytes > w.partial_bytes || counters > w.counter_count;
   if (grow) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(NVFP4_ERR_INVALID_ARG,
+                  "split-K workspace must grow while the stream is being captured; run the same "
+                  "problem once on this stream before capturing it");
     // the old buffers may still be in use by work queued on this stream
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     cudaFree(w.partials);

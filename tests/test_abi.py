@@ -64,9 +64,11 @@ def test_plan_single_tile_and_full_machine(lib):
 def test_plan_splits_skinny_problem(lib):
     p = binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)
     s = p["splits"][0]
-    assert s > 1 and p["units"] == 56 * s
-    assert p["units"] / (-(-p["units"] // 152) * 152) > 0.9      # waves nearly full
-    assert 64 // s >= 4                                          # >= 4 k-tiles per unit
+    assert s == 2 and p["units"] == 112 and p["grid"] == 112    # one wave of units
+    p = binding.nvfp4_gemm_plan([128], [512], [4096], [1], 152)
+    assert p["splits"] == [4]                                    # capped: >= 4 k-tiles per unit
+    p = binding.nvfp4_gemm_plan([128], [128], [256], [1], 152)
+    assert p["splits"] == [1]
 
 
 def test_plan_grouped(lib):

@@ -11,7 +11,7 @@ from gpu_util import alloc_c, assert_close_full, require_gpu, run_single, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("shape,skip", [((128, 128, 256, 1), 0), ((128, 512, 4096, 1), 5)])
+@pytest.mark.parametrize("shape,skip", [((128, 128, 256, 1), 0), ((128, 512, 4096, 1), 2)])
 def test_timeout_is_reported_and_context_survives(shape, skip):
     binding = require_gpu()
     p = workloads.make_random_problem(77, *shape)
