@@ -168,13 +168,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Largest value over all ranks (the job takes as long as its slowest rank)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(flops_per_step, steps, elapsed_ms_max, world):
+    """Whole-job TFLOP/s under weak scaling: every rank ran `steps` steps of
+    the same workload; the job took the slowest rank's time."""
+    return flops_per_step * steps * world / (elapsed_ms_max * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -422,7 +429,7 @@ def main():
     # ---- numbers
     flops = wl.flops
     ms_per_step = elapsed_ms / args.steps
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, elapsed_ms, world)
     peaks, peak_src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     fp4_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP4_OVER_BF16
