@@ -53,6 +53,8 @@ def load_library(path=LIB_PATH):
     lib.nvfp4_gemm_repack_scales.restype = i
     lib.nvfp4_gemm_run.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
     lib.nvfp4_gemm_run.restype = i
+    lib.nvfp4_gemm_run_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, vp]
+    lib.nvfp4_gemm_run_noalloc.restype = i
     lib.nvfp4_gemm_run_grouped.argtypes = [i, vpp, vpp, vpp, vpp, vpp, ip, ip, ip, ip, vp]
     lib.nvfp4_gemm_run_grouped.restype = i
     lib.nvfp4_gemm_last_error_string.argtypes = []
@@ -116,6 +118,14 @@ def nvfp4_gemm_run(A, B, SFA, SFB, C, M, N, K, L=1, stream=None):
     rc = load_library().nvfp4_gemm_run(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K, L,
                                        _stream(stream))
     _check(rc, "nvfp4_gemm_run")
+
+
+def nvfp4_gemm_run_noalloc(A, B, SFA, SFB, C, M, N, K, L=1, stream=None):
+    """nvfp4_gemm_run for callers that cannot allocate device memory: the
+    split-K scratch is a static device array (see include/nvfp4_gemm.h)."""
+    rc = load_library().nvfp4_gemm_run_noalloc(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
+                                               L, _stream(stream))
+    _check(rc, "nvfp4_gemm_run_noalloc")
 
 
 def nvfp4_gemm_run_grouped(G, A, B, SFA, SFB, C, M, N, K, L, stream=None):

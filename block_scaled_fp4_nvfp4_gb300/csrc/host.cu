@@ -480,3 +480,127 @@ uint64_t nvfp4_gemm_encode_smem_desc(uint32_t smem_addr, int swizzle128) {
 }
 
 }  // extern "C"
+
+// =================================================================== no-allocation variant
+// For callers that must not allocate device memory: code running where
+// cudaMalloc is forbidden or unsafe (inside a host callback or a custom
+// allocator, a runtime that owns every byte of the device heap, or a process
+// that only gets a fixed memory budget at start-up).  This variant of
+// nvfp4_gemm_run keeps its split-K scratch (partial tiles, arrival counters,
+// status word) in one static device array that every device loading this
+// library reserves until the process exits, and it calls no allocator.
+namespace {
+
+// Largest split-K partial area the static array holds: one wave of 128x128
+// fp32 partial tiles on a 160-SM device (the planner never puts more units
+// than SMs into a split launch).
+constexpr size_t kNoAllocPartialBytes = 160ull * kBM * 128 * sizeof(float);  // 10 MiB
+constexpr int kNoAllocCounters = 4096;       // output tiles of one split launch
+constexpr size_t kNoAllocHeader = 256;       // status word, padded
+constexpr size_t kNoAllocCounterBytes = kNoAllocCounters * sizeof(int);
+constexpr size_t kNoAllocBytes = kNoAllocHeader + kNoAllocCounterBytes + kNoAllocPartialBytes;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  int sms = 0;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+std::map<int, NoAllocDevice> g_noalloc_devices;
+
+// One-time set-up per device, made with that device current.  The symbol's
+// host-side name is only a stand-in; the device address comes from the runtime.
+int noalloc_setup(int dev, NoAllocDevice** out) {
+  NoAllocDevice& d = g_noalloc_devices[dev];
+  if (!d.ready) {
+    cudaError_t e;
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    if (major != 10 || minor != 3)
+      return fail(NVFP4_ERR_UNSUPPORTED_DEVICE,
+                  "device %d has compute capability %d.%d; this library is built for sm_103a only", dev,
+                  major, minor);
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    if ((e = gemm_prepare_device(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    d.scratch = static_cast<unsigned char*>(ptr);
+    d.ready = true;
+  }
+  *out = &d;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* SFA, const void* SFB,
+                                      void* C, int M, int N, int K, int L, void* stream_) {
+  int rc = check_shapes(1, &M, &N, &K, &L);
+  if (rc != NVFP4_OK) return rc;
+  if (!A || !B || !SFA || !SFB || !C) return fail(NVFP4_ERR_INVALID_ARG, "null device pointer");
+  if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB) || !aligned16(C))
+    return fail(NVFP4_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  NoAllocDevice* nd = nullptr;
+  if ((rc = noalloc_setup(dev, &nd)) != NVFP4_OK) return rc;
+
+  Plan pl;
+  if ((rc = make_plan(1, &M, &N, &K, &L, nd->sms, &pl)) != NVFP4_OK) return rc;
+  const bool split = pl.splits[0] > 1;
+  const size_t partial_bytes = split ? static_cast<size_t>(pl.total_units) * kBM * pl.bn * sizeof(float) : 0;
+  if (partial_bytes > kNoAllocPartialBytes || (split && pl.total_tiles > kNoAllocCounters))
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "this problem needs %zu bytes of split-K scratch and %d tile counters; the static "
+                "no-allocation area holds %zu bytes and %d counters",
+                partial_bytes, pl.total_tiles, kNoAllocPartialBytes, kNoAllocCounters);
+
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  if ((rc = encode_operand_map(&p.tmA[0], A, M, K, L, kBM)) != NVFP4_OK) return rc;
+  if ((rc = encode_operand_map(&p.tmB[0], B, N, K, L, pl.bn)) != NVFP4_OK) return rc;
+  if ((rc = encode_c_map(&p.tmC[0], C, M, N, L)) != NVFP4_OK) return rc;
+  p.sfa[0] = static_cast<const uint8_t*>(SFA);
+  p.sfb[0] = static_cast<const uint8_t*>(SFB);
+  p.M[0] = M;
+  p.N[0] = N;
+  p.L[0] = L;
+  p.ktiles[0] = K / kBK;
+  p.tiles_m[0] = pl.tiles_m[0];
+  p.tiles_n[0] = pl.tiles_n[0];
+  p.splits[0] = pl.splits[0];
+  p.sf_rows_a[0] = static_cast<int>(cdiv(M, 128));
+  p.sf_rows_b[0] = static_cast<int>(cdiv(N, 128));
+  p.a_streams[0] = M > N ? 1 : 0;
+  p.unit_start[0] = pl.unit_start[0];
+  p.unit_start[1] = pl.unit_start[1];
+  p.tile_start[0] = pl.tile_start[0];
+  p.tile_start[1] = pl.tile_start[1];
+  p.num_groups = 1;
+  p.total_units = pl.total_units;
+  p.timeout_ns = g_timeout_ns.load();
+  p.debug_skip_ktile = -1;
+  p.status = reinterpret_cast<int*>(nd->scratch);
+  p.counters = reinterpret_cast<int*>(nd->scratch + kNoAllocHeader);
+  p.workspace = reinterpret_cast<float*>(nd->scratch + kNoAllocHeader + kNoAllocCounterBytes);
+
+  // The array keeps whatever the previous call left: the status word and the
+  // counters this launch uses must start at zero (the partial tiles are always
+  // written before they are read).
+  const size_t clear = kNoAllocHeader + (split ? static_cast<size_t>(pl.total_tiles) * sizeof(int) : 0);
+  if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
+  e = gemm_launch(pl.bn, p, pl.grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  return ok();
+}

@@ -153,6 +153,35 @@ NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, c
                     int num_sms, int* out, int out_len);
 
 /*
+ * nvfp4_gemm_run without any device allocation.  The source pages have no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running inside a host callback or a custom allocator, a
+ * runtime that owns the whole device heap, or a process held to a fixed
+ * memory budget -- and so cannot let the library create its split-K
+ * workspace on first use.
+ *
+ * Same arguments, layouts, shape contract and result as nvfp4_gemm_run (one
+ * problem).  Split-K scratch (fp32 partial tiles, per-tile arrival counters,
+ * a status word) lives in one static device array of 10 MiB + 16.25 KiB that
+ * every device which loads this library holds until the process exits.  The
+ * first call on a device (with that device current) looks up the array's
+ * device address once; make that first call before capturing any stream.
+ * Each call clears the counters and status word it uses (an asynchronous
+ * memset on `stream`) and calls no allocator.
+ *
+ * All calls share the one array: calls whose work may overlap on the GPU
+ * (different streams, or different host threads) race on it and give wrong
+ * results; order them on one stream.  A problem whose split-K plan needs more
+ * than the array holds returns NVFP4_ERR_UNSUPPORTED_SHAPE with the sizes in
+ * the error string.  A bounded device wait that runs out ends the kernel early
+ * and leaves C undefined; in this variant the timeout is recorded only in the
+ * array's own status word, which the next call clears.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, UNSUPPORTED_DEVICE, CUDA.
+ */
+NVFP4_API int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* SFA, const void* SFB,
+                                     void* C, int M, int N, int K, int L, void* stream);
+
+/*
  * Descriptor encoders used by the kernel, exported for host-side checks.
  *   nvfp4_gemm_encode_idesc: tcgen05.mma kind::mxf4nvf4 instruction
  *     descriptor for E2M1 x E2M1 with E4M3 block-16 scales, K-major operands.

@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = binding.header_functions()
-    assert len(names) == 11
+    assert len(names) == 12
     for n in names:
         assert hasattr(lib, n), n
         ctypes.cast(getattr(lib, n), ctypes.c_void_p)
