@@ -67,6 +67,8 @@ def load_library(path=LIB_PATH):
     lib.nvfp4_gemm_debug_inject_skip.restype = i
     lib.nvfp4_gemm_plan.argtypes = [i, ip, ip, ip, ip, i, ip, i]
     lib.nvfp4_gemm_plan.restype = i
+    lib.nvfp4_gemm_debug_schedule.argtypes = [i, ip, ip, ip, ip, i, i, ip, i]
+    lib.nvfp4_gemm_debug_schedule.restype = i
     lib.nvfp4_gemm_encode_idesc.argtypes = [i, i]
     lib.nvfp4_gemm_encode_idesc.restype = ctypes.c_uint32
     lib.nvfp4_gemm_encode_smem_desc.argtypes = [ctypes.c_uint32, i]
@@ -165,13 +167,28 @@ def nvfp4_gemm_debug_inject_skip(ktile):
 
 
 def nvfp4_gemm_plan(M, N, K, L, num_sms):
-    """Host-only launch plan: dict(bn, units, grid, stages, splits)."""
+    """Host-only launch plan (see include/nvfp4_gemm.h) as a dict."""
     G = len(M)
     ia = lambda xs: (ctypes.c_int * G)(*[int(v) for v in xs])
-    out = (ctypes.c_int * (4 + G))()
-    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 4 + G)
+    out = (ctypes.c_int * 8)()
+    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 8)
     _check(rc, "nvfp4_gemm_plan")
-    return dict(bn=out[0], units=out[1], grid=out[2], stages=out[3], splits=list(out[4:4 + G]))
+    keys = ("bn", "tiles", "grid", "stages", "dp_tiles", "sk_tiles", "sk_iters", "sk_max_segs")
+    return dict(zip(keys, list(out)))
+
+
+def nvfp4_gemm_debug_schedule(M, N, K, L, num_sms, cta):
+    """Host-only work list of one CTA: list of dicts (g, l, tm, tn, kt0, kt1,
+    tile, seg, nseg)."""
+    G = len(M)
+    ia = lambda xs: (ctypes.c_int * G)(*[int(v) for v in xs])
+    cap = 9 * 4096
+    out = (ctypes.c_int * cap)()
+    n = load_library().nvfp4_gemm_debug_schedule(G, ia(M), ia(N), ia(K), ia(L), num_sms, cta, out, cap)
+    if n < 0:
+        _check(n, "nvfp4_gemm_debug_schedule")
+    keys = ("g", "l", "tm", "tn", "kt0", "kt1", "tile", "seg", "nseg")
+    return [dict(zip(keys, out[9 * i:9 * i + 9])) for i in range(min(n, cap // 9))]
 
 
 def nvfp4_gemm_encode_idesc(M, N):

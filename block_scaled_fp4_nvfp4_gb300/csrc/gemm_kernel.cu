@@ -31,6 +31,7 @@
 #include "descriptors.h"
 #include "gemm_params.h"
 #include "ptx.cuh"
+#include "schedule.h"
 
 namespace nvfp4 {
 
@@ -50,31 +51,6 @@ struct SmemCtl {
   volatile int abort;
   int last_flag;
 };
-
-struct Unit {
-  int g, l, tm, tn, split, splits, kt0, kt1, tile;
-};
-
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u) {
-  int g = 0;
-  while (g + 1 < p.num_groups && u >= p.unit_start[g + 1]) ++g;
-  const int r = u - p.unit_start[g];
-  const int S = p.splits[g];
-  Unit x;
-  x.g = g;
-  x.splits = S;
-  x.split = r % S;
-  const int t = r / S;  // tile index inside the group, m fastest
-  x.tm = t % p.tiles_m[g];
-  const int rest = t / p.tiles_m[g];
-  x.tn = rest % p.tiles_n[g];
-  x.l = rest / p.tiles_n[g];
-  const int KT = p.ktiles[g];
-  x.kt0 = static_cast<int>(static_cast<long long>(KT) * x.split / S);
-  x.kt1 = static_cast<int>(static_cast<long long>(KT) * (x.split + 1) / S);
-  x.tile = p.tile_start[g] + t;
-  return x;
-}
 
 // Bounded mbarrier wait.  Returns false if the CTA is aborting or the limit
 // ran out (then the abort flag and the device status word are set).
@@ -170,7 +146,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int g = 0; g < p.num_groups; ++g) {
+    for (int g = 0; g < p.sched.num_groups; ++g) {
       ptx::prefetch_tensormap(&p.tmA[g]);
       ptx::prefetch_tensormap(&p.tmB[g]);
       ptx::prefetch_tensormap(&p.tmC[g]);
@@ -184,6 +160,32 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
+
+  // Programmatic dependent launch: everything above overlaps the previous
+  // kernel on the stream.  Before waiting for it, one thread asks L2 for the
+  // first k-tiles this CTA will load (operand tiles and scale slabs), so HBM
+  // stays busy while the previous kernel drains; every actual load and store
+  // comes after the wait.
+  if (warp == 0 && lane == 0 && p.prefetch_ktiles > 0) {
+    WorkCursor pc;
+    work_begin(p.sched, blockIdx.x, gridDim.x, pc);
+    Work pw;
+    int left = p.prefetch_ktiles;
+    while (left > 0 && work_next(p.sched, blockIdx.x, gridDim.x, pc, pw)) {
+      const size_t atoms = static_cast<size_t>(p.sched.ktiles[pw.g]) * 4;
+      const uint8_t* sfa = p.sfa[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_a[pw.g] + pw.tm) * atoms * kSfAtomBytes;
+      const int sfb_block0 = pw.tn * Cfg::kSfbBlocks;
+      const uint8_t* sfb = p.sfb[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_b[pw.g] + sfb_block0) * atoms * kSfAtomBytes;
+      for (int kt = pw.kt0; kt < pw.kt1 && left > 0; ++kt, --left) {
+        ptx::prefetch_tile_l2_3d(&p.tmA[pw.g], kt * kBKBytes, pw.tm * kBM, pw.l);
+        ptx::prefetch_tile_l2_3d(&p.tmB[pw.g], kt * kBKBytes, pw.tn * BN, pw.l);
+        ptx::prefetch_l2(sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
+        if (sfb_block0 < p.sf_rows_b[pw.g]) ptx::prefetch_l2(sfb + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
+      }
+    }
+  }
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   const Waiter W{&ctl.abort, p.status, p.timeout_ns};
 
@@ -200,13 +202,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     for (int s = 0; s < kStages; ++s) armed[s] = -1;
     int count = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-      const Unit x = decode_unit(p, u);
+    WorkCursor cur;
+    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    Work x;
+    while (ok && work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
       const CUtensorMap* mapA = &p.tmA[x.g];
       const CUtensorMap* mapB = &p.tmB[x.g];
       const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
       const uint64_t polB = p.a_streams[x.g] ? pol_keep : pol_stream;
-      const size_t atoms_per_block = static_cast<size_t>(p.ktiles[x.g]) * 4;
+      const size_t atoms_per_block = static_cast<size_t>(p.sched.ktiles[x.g]) * 4;
       const uint8_t* sfa = p.sfa[x.g] +
           (static_cast<size_t>(x.l) * p.sf_rows_a[x.g] + x.tm) * atoms_per_block * kSfAtomBytes;
       const int sfb_block0 = x.tn * Cfg::kSfbBlocks;
@@ -265,8 +269,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int ab = 0;
     uint32_t aphase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-      const Unit x = decode_unit(p, u);
+    WorkCursor cur;
+    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    Work x;
+    while (ok && work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
       if (!warp_wait(W, acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
         ok = false;
         break;
@@ -338,7 +344,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int buf = 0;
     // Convert 64 fp32 columns of this thread's row to fp16, stage them as one
     // 128-byte swizzled row of a 32 x 64 box and let lane 0 store the box.
-    auto store_chunk = [&](const Unit& x, int q, const float* v) {
+    auto store_chunk = [&](const Work& x, int q, const float* v) {
       const uint32_t sbuf = epi_base + (ew * 2 + buf) * Cfg::kEpiBufBytes;
       if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this buffer is done
       __syncwarp();
@@ -369,8 +375,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
     };
 
-    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-      const Unit x = decode_unit(p, u);
+    WorkCursor cur;
+    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    Work x;
+    while (work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
       if (!warp_wait(W, acc_full_bar(ab), aphase, kStatusTimeoutEpilogue)) break;
       ptx::tc_fence_after_sync();
       const uint32_t t_row = tmem + (static_cast<uint32_t>(sub * 32) << 16) + ab * BN;
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         if (lane == 0) ptx::mbar_arrive(acc_empty_bar(my_ab));
       };
 
-      if (x.splits == 1) {
+      if (x.nseg == 1) {
 #pragma unroll 1
         for (int q = 0; q < BN / 64; ++q) {
           float v[64];
@@ -397,27 +405,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         continue;
       }
 
-      // Split-K: publish this split's partial tile, column-major so that a
-      // warp's stores of one column are 128 contiguous bytes.
-      float* ws = p.workspace + static_cast<size_t>(u) * (BN * kBM) + row;
+      // Stream-K segment: publish this partial tile as [BN/4][128 rows][4]
+      // fp32, so each thread stores (and later loads) 16 bytes of its row and
+      // a warp touches 512 contiguous bytes per column group.
+      float4* ws = reinterpret_cast<float4*>(p.workspace) + sk_slot(p.sched, x, x.seg) * (BN / 4 * kBM) + row;
 #pragma unroll 1
       for (int q = 0; q < BN / 64; ++q) {
         float v[64];
         load_chunk(t_row + 64 * q, v);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) __stcg(ws + (64 * q + c) * kBM, v[c]);
+        for (int c4 = 0; c4 < 16; ++c4)
+          __stcg(ws + (16 * q + c4) * kBM, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
       }
       release_acc();
       __threadfence();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(gather_bar);
       bool ok = true;
+      const int ctr = sk_counter(p.sched, x);
       if (ew == 0) {
         ok = warp_wait(W, gather_bar, gphase, kStatusTimeoutEpilogue);
         if (ok && lane == 0) {
           __threadfence();
-          const int old = atomicAdd(&p.counters[x.tile], 1);
-          const int last = (old == x.splits - 1) ? 1 : 0;
+          const int old = atomicAdd(&p.counters[ctr], 1);
+          const int last = (old == x.nseg - 1) ? 1 : 0;
           if (last) __threadfence();
           ctl.last_flag = last;
           ptx::mbar_arrive(bcast_bar);
@@ -429,22 +440,58 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       gphase ^= 1u;
       if (!ctl.last_flag) continue;
       __threadfence();
-      // Last arrival: sum the partials of splits 0..S-1 in that order, so the
-      // result does not depend on which split finished last.
-      const float* ws0 = p.workspace + static_cast<size_t>(u - x.split) * (BN * kBM) + row;
+      // Last segment to finish: sum the segments' partials in k order (0, 1,
+      // ...), so the result does not depend on which segment finished last.
+      const float4* ws0 = reinterpret_cast<const float4*>(p.workspace) + sk_slot(p.sched, x, 0) * (BN / 4 * kBM) + row;
+      constexpr int kMaxSeg = 4;  // loads of up to 4 segments in flight at once
 #pragma unroll 1
       for (int q = 0; q < BN / 64; ++q) {
         float v[64];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) v[c] = 0.0f;
-        for (int j = 0; j < x.splits; ++j) {
-          const float* src = ws0 + static_cast<size_t>(j) * (BN * kBM) + (64 * q) * kBM;
+        for (int h = 0; h < 2; ++h) {  // 32-column halves
+          float4 acc[8];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) v[c] += __ldcg(src + c * kBM);
+          for (int c4 = 0; c4 < 8; ++c4) acc[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j0 = 0; j0 < x.nseg; j0 += kMaxSeg) {
+            float4 part[kMaxSeg][8];
+#pragma unroll
+            for (int j = 0; j < kMaxSeg; ++j)
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4)
+                part[j][c4] = (j0 + j < x.nseg)
+                    ? __ldcg(ws0 + static_cast<size_t>(j0 + j) * (BN / 4 * kBM) + (16 * q + 8 * h + c4) * kBM)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kMaxSeg; ++j)
+              if (j0 + j < x.nseg)
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                  acc[c4].x += part[j][c4].x;
+                  acc[c4].y += part[j][c4].y;
+                  acc[c4].z += part[j][c4].z;
+                  acc[c4].w += part[j][c4].w;
+                }
+          }
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            v[32 * h + 4 * c4] = acc[c4].x;
+            v[32 * h + 4 * c4 + 1] = acc[c4].y;
+            v[32 * h + 4 * c4 + 2] = acc[c4].z;
+            v[32 * h + 4 * c4 + 3] = acc[c4].w;
+          }
         }
         if (rows_live) store_chunk(x, q, v);
       }
-      if (ew == 0 && lane == 0) p.counters[x.tile] = 0;  // ready for the next launch
+      // The partials are consumed: drop their L2 lines without writing them
+      // back.  This warp read exactly the lines of its own 32 rows.
+      __syncwarp();
+      for (int j = 0; j < x.nseg; ++j) {
+        const char* base = reinterpret_cast<const char*>(
+            reinterpret_cast<const float4*>(p.workspace) + sk_slot(p.sched, x, j) * (BN / 4 * kBM) + sub * 32);
+        for (int line = lane; line < (BN / 4) * 4; line += 32)  // (BN/4) column groups x 4 lines of 128 B
+          ptx::discard_l2(base + static_cast<size_t>(line >> 2) * (kBM * 16) + (line & 3) * 128);
+      }
+      if (ew == 0 && lane == 0) p.counters[ctr] = 0;  // ready for the next launch
     }
     if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();
@@ -458,13 +505,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
 // ---------------------------------------------------------------- launcher
 template <int BN>
-static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream) {
+static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   using Cfg = TileCfg<BN>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kDynSmem;
   cfg.stream = stream;
+  // Programmatic dependent launch: this grid may start while the previous
+  // kernel on the stream finishes; the kernel waits for it (griddepcontrol)
+  // before its first global-memory access.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN>, p);
 }
 
@@ -481,9 +536,9 @@ cudaError_t gemm_prepare_device(int bn) {
   }
 }
 
-cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream) {
+cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   switch (bn) {
-    case 128: return launch_bn<128>(p, grid, stream);
+    case 128: return launch_bn<128>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "schedule.h"
+
 namespace nvfp4 {
 
 constexpr int kMaxGroups = 8;
@@ -38,22 +40,17 @@ struct GemmParams {
   CUtensorMap tmC[kMaxGroups];   // fp16 {N, M, L}, box {64, 32, 1}, 128B swizzle
   const uint8_t* sfa[kMaxGroups];  // repacked scales
   const uint8_t* sfb[kMaxGroups];
-  int M[kMaxGroups], N[kMaxGroups], L[kMaxGroups];
-  int ktiles[kMaxGroups];        // K / 256
-  int tiles_m[kMaxGroups], tiles_n[kMaxGroups];
-  int splits[kMaxGroups];        // split-K factor (1 = whole K per unit)
+  int M[kMaxGroups], N[kMaxGroups];
   int sf_rows_a[kMaxGroups];     // ceil(M/128): 128-row scale blocks per batch
   int sf_rows_b[kMaxGroups];     // ceil(N/128)
   int a_streams[kMaxGroups];     // 1: A is the streamed operand (evict-first), B kept
-  int unit_start[kMaxGroups + 1];  // prefix over groups of work units
-  int tile_start[kMaxGroups + 1];  // prefix over groups of output tiles
-  int num_groups;
-  int total_units;
-  float* workspace;              // split-K partials, [unit][BN][128] fp32
-  int* counters;                 // per output tile arrival counters (zero between launches)
+  Schedule sched;                // data-parallel + stream-K work decomposition
+  float* workspace;              // stream-K partials, [slot][BN/4][128][4] fp32
+  int* counters;                 // per stream-K tile arrival counters (zero between launches)
   int* status;                   // device status word
   unsigned long long timeout_ns; // limit of every bounded wait
   int debug_skip_ktile;          // test-only fault injection (-1 = off)
+  int prefetch_ktiles;           // k-tiles per CTA prefetched into L2 before the launch dependency wait
 };
 
 // Per-BN compile-time configuration.

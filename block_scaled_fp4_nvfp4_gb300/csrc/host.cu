@@ -25,10 +25,11 @@
 #include "../../include/nvfp4_gemm.h"
 #include "descriptors.h"
 #include "gemm_params.h"
+#include "schedule.h"
 
 namespace nvfp4 {
 cudaError_t gemm_prepare_device(int bn);
-cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
 int gemm_stages(int bn);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
 }  // namespace nvfp4
@@ -193,69 +194,131 @@ int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
 struct Plan {
   int bn = 128;
   int stages = 0;
-  int total_units = 0;
-  int total_tiles = 0;
   int grid = 0;
-  int splits[kMaxGroups] = {};
   int tiles_m[kMaxGroups] = {}, tiles_n[kMaxGroups] = {};
-  int unit_start[kMaxGroups + 1] = {};
-  int tile_start[kMaxGroups + 1] = {};
+  Schedule sched = {};
+  size_t workspace_bytes = 0;  // stream-K partials
+  int counters = 0;            // stream-K tiles
 };
 
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
-// Split-K only when the output tiles do not fill the machine.  Measured on
-// GB300 (128 x 7168 x 16384): splits beyond one wave of units cost more in
-// partial-tile traffic and reduction than they gain in parallelism, so S is
-// the largest factor that keeps tiles * S within one wave, with at least 4
-// k-tiles per unit.
-int choose_split(long long tiles, const int* ktiles, int G, int sms) {
-  if (tiles >= sms) return 1;
-  int min_kt = ktiles[0];
-  for (int g = 1; g < G; ++g) min_kt = ktiles[g] < min_kt ? ktiles[g] : min_kt;
-  const int max_s = min_kt / 4 < 1 ? 1 : (min_kt / 4 > 32 ? 32 : min_kt / 4);
-  long long s = sms / tiles;
-  if (s > max_s) s = max_s;
-  return s < 1 ? 1 : static_cast<int>(s);
+// k-tiles each CTA prefetches into L2 before waiting for the preceding kernel
+// (NVFP4_PREFETCH overrides; 0 disables).
+int prefetch_ktiles() {
+  if (const char* env = getenv("NVFP4_PREFETCH")) {
+    const int v = atoi(env);
+    if (v >= 0 && v <= 64) return v;
+  }
+  return 6;
 }
+
+enum SchedMode { kSchedAuto = 0, kSchedDataParallel = 1, kSchedStreamK = 2 };
+
+// Tuning / test override of the decomposition: NVFP4_SCHEDULE = dp | sk | auto.
+SchedMode sched_mode() {
+  const char* env = getenv("NVFP4_SCHEDULE");
+  if (!env) return kSchedAuto;
+  if (strcmp(env, "dp") == 0) return kSchedDataParallel;
+  if (strcmp(env, "sk") == 0) return kSchedStreamK;
+  return kSchedAuto;
+}
+
+// Decomposition.  With at least one wave of output tiles every tile runs
+// whole (data-parallel, one per CTA per wave).  With fewer tiles than SMs the
+// tiles' k-tiles are shared out (stream-K) over tiles x S CTAs, S the largest
+// factor that keeps tiles x S within the SMs and at least kMinSkIters k-tiles
+// per CTA, so every tile is cut into S aligned, equal segments.  Measured on
+// GB300: for 128 x 7168 x 16384 two equal segments per tile (112 CTAs) beat
+// 152 CTAs with uneven ranges (22.6 vs 23.8 us); for the grouped workloads a
+// stream-K tail after the full waves cost more in partial traffic than the
+// ragged last wave (MoE 8 groups: 70.8 vs 61.7 us), so no hybrid by default.
+// NVFP4_SCHEDULE=sk forces stream-K over all tiles with one CTA per SM.
+constexpr int kMinSkIters = 4;
 
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl) {
   pl->bn = 128;
   pl->stages = gemm_stages(pl->bn);
-  int ktiles[kMaxGroups];
+  Schedule& s = pl->sched;
+  memset(&s, 0, sizeof s);
+  s.num_groups = G;
   long long tiles = 0;
   for (int g = 0; g < G; ++g) {
-    ktiles[g] = K[g] / kBK;
     pl->tiles_m[g] = static_cast<int>(cdiv(M[g], kBM));
     pl->tiles_n[g] = static_cast<int>(cdiv(N[g], pl->bn));
+    s.tiles_m[g] = pl->tiles_m[g];
+    s.tiles_n[g] = pl->tiles_n[g];
+    s.L[g] = L[g];
+    s.ktiles[g] = K[g] / kBK;
+    s.tile_start[g] = static_cast<int>(tiles);
     tiles += static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
+    if (tiles > 0x3FFFFFFFLL) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "problem has too many output tiles");
   }
-  int s = choose_split(tiles, ktiles, G, sms);
-  // Tuning / test override of the split-K factor (capped per group below).
-  if (const char* env = getenv("NVFP4_SPLIT_K")) {
-    const int v = atoi(env);
-    if (v >= 1 && v <= 64) s = v;
-  }
-  long long units = 0, tcount = 0;
+  s.tile_start[G] = static_cast<int>(tiles);
+  s.total_tiles = static_cast<int>(tiles);
+
+  const SchedMode mode = sched_mode();
+  long long dp = tiles;  // data-parallel tiles
+  if (mode == kSchedStreamK || (mode == kSchedAuto && tiles < sms)) dp = 0;
+  s.dp_tiles = static_cast<int>(dp);
+
+  // stream-K iteration space: the remaining tiles' k-tiles, group by group
+  long long T = 0;
   for (int g = 0; g < G; ++g) {
-    const long long tg = static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
-    int sg = s;
-    const int cap = ktiles[g] / 4 < 1 ? 1 : ktiles[g] / 4;
-    if (sg > cap) sg = cap;
-    if (sg > ktiles[g]) sg = ktiles[g];
-    pl->splits[g] = sg;
-    pl->unit_start[g] = static_cast<int>(units);
-    pl->tile_start[g] = static_cast<int>(tcount);
-    units += tg * sg;
-    tcount += tg;
-    if (units > 0x7FFFFFFFLL || tcount > 0x7FFFFFFFLL)
-      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "problem has too many output tiles");
+    const long long first = s.dp_tiles > s.tile_start[g] ? s.dp_tiles : s.tile_start[g];
+    const long long count = s.tile_start[g + 1] > first ? s.tile_start[g + 1] - first : 0;
+    s.sk_tile_first[g] = static_cast<int>(first);
+    s.sk_iter_start[g] = T;
+    T += count * s.ktiles[g];
   }
-  pl->unit_start[G] = static_cast<int>(units);
-  pl->tile_start[G] = static_cast<int>(tcount);
-  pl->total_units = static_cast<int>(units);
-  pl->total_tiles = static_cast<int>(tcount);
-  pl->grid = static_cast<int>(units < sms ? units : sms);
+  s.sk_iter_start[G] = T;
+  s.sk_iters = T;
+
+  if (T > 0) {
+    long long grid = sms;
+    if (mode == kSchedAuto) {
+      // equal aligned segments: S per tile, S | gcd of the groups' k-tile counts
+      int kt_min = s.ktiles[0];
+      for (int g = 1; g < G; ++g) kt_min = s.ktiles[g] < kt_min ? s.ktiles[g] : kt_min;
+      long long S = sms / tiles;
+      if (S > kt_min / kMinSkIters) S = kt_min / kMinSkIters;
+      for (; S > 1; --S) {
+        bool divides = true;
+        for (int g = 0; g < G; ++g) divides = divides && (s.ktiles[g] % S == 0);
+        if (divides) break;
+      }
+      if (S < 1) S = 1;
+      // equal segments need every tile to have the same number of k-tiles
+      bool same_kt = true;
+      for (int g = 1; g < G; ++g) same_kt = same_kt && s.ktiles[g] == s.ktiles[0];
+      grid = same_kt ? tiles * S : sms;
+    }
+    if (dp == 0 && T / kMinSkIters < grid) grid = T / kMinSkIters > 0 ? T / kMinSkIters : 1;
+    if (dp == 0)
+      if (const char* env = getenv("NVFP4_SK_GRID")) {  // tuning override (stream-K only plans)
+        const long long v = atoll(env);
+        if (v >= 1 && v <= sms) grid = v;
+      }
+    pl->grid = static_cast<int>(grid);
+    // exact largest number of CTAs covering one stream-K tile
+    int max_segs = 1;
+    for (int g = 0; g < G; ++g) {
+      const long long n = s.tile_start[g + 1] - s.sk_tile_first[g];
+      for (long long i = 0; i < n; ++i) {
+        const long long b = s.sk_iter_start[g] + i * s.ktiles[g];
+        const int segs = sk_owner(b + s.ktiles[g] - 1, T, pl->grid) - sk_owner(b, T, pl->grid) + 1;
+        if (segs > max_segs) max_segs = segs;
+      }
+    }
+    s.sk_max_segs = max_segs;
+    pl->counters = static_cast<int>(tiles - dp);
+    pl->workspace_bytes = max_segs > 1 ? static_cast<size_t>(tiles - dp) * max_segs * kBM * pl->bn * sizeof(float) : 0;
+  } else {
+    pl->grid = static_cast<int>(tiles < sms ? tiles : sms);
+    s.sk_max_segs = 1;
+    pl->counters = 0;
+    pl->workspace_bytes = 0;
+  }
   if (pl->grid < 1) pl->grid = 1;
   return NVFP4_OK;
 }
@@ -305,6 +368,9 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t cou
     if ((e = cudaMalloc(&w.partials, pb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K workspace)");
     if ((e = cudaMalloc(&w.counters, cb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K counters)");
     if ((e = cudaMemsetAsync(w.counters, 0, cb, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    // the next launch may overlap its predecessor (programmatic dependent
+    // launch): make sure the zeroed counters are in place first
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     w.partial_bytes = pb;
     w.counter_count = cb / sizeof(int);
   }
@@ -371,11 +437,6 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.sfb[g] = static_cast<const uint8_t*>(SFB[g]);
     p.M[g] = M[g];
     p.N[g] = N[g];
-    p.L[g] = L[g];
-    p.ktiles[g] = K[g] / kBK;
-    p.tiles_m[g] = pl.tiles_m[g];
-    p.tiles_n[g] = pl.tiles_n[g];
-    p.splits[g] = pl.splits[g];
     p.sf_rows_a[g] = static_cast<int>(cdiv(M[g], 128));
     p.sf_rows_b[g] = static_cast<int>(cdiv(N[g], 128));
     // The larger operand streams through L2 once (evict-first); the smaller,
@@ -383,27 +444,20 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     // Same rule as "nvfp4 group gemm, submission 407526" (cache_A / cache_B).
     p.a_streams[g] = M[g] > N[g] ? 1 : 0;
   }
-  for (int g = 0; g <= G; ++g) {
-    p.unit_start[g] = pl.unit_start[g];
-    p.tile_start[g] = pl.tile_start[g];
-  }
-  p.num_groups = G;
-  p.total_units = pl.total_units;
+  p.sched = pl.sched;
+  p.prefetch_ktiles = prefetch_ktiles();
   p.status = ds->status;
   p.timeout_ns = g_timeout_ns.load();
   p.debug_skip_ktile = g_debug_skip.exchange(-1);
 
-  bool any_split = false;
-  for (int g = 0; g < G; ++g) any_split |= pl.splits[g] > 1;
-  if (any_split) {
+  if (pl.workspace_bytes > 0) {
     Workspace* w = nullptr;
-    const size_t partial_bytes = static_cast<size_t>(pl.total_units) * kBM * pl.bn * sizeof(float);
-    if ((rc = get_workspace(dev, stream, partial_bytes, pl.total_tiles, &w)) != NVFP4_OK) return rc;
+    if ((rc = get_workspace(dev, stream, pl.workspace_bytes, pl.counters, &w)) != NVFP4_OK) return rc;
     p.workspace = w->partials;
     p.counters = w->counters;
   }
 
-  e = gemm_launch(pl.bn, p, pl.grid, stream);
+  e = gemm_launch(pl.bn, p, pl.grid, stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }
@@ -462,15 +516,42 @@ int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* 
                     int out_len) {
   int rc = check_shapes(G, M, N, K, L);
   if (rc != NVFP4_OK) return rc;
-  if (num_sms < 1 || !out || out_len < 4 + G) return fail(NVFP4_ERR_INVALID_ARG, "bad plan arguments");
+  if (num_sms < 1 || !out || out_len < 8) return fail(NVFP4_ERR_INVALID_ARG, "bad plan arguments");
   Plan pl;
   if ((rc = make_plan(G, M, N, K, L, num_sms, &pl)) != NVFP4_OK) return rc;
   out[0] = pl.bn;
-  out[1] = pl.total_units;
+  out[1] = pl.sched.total_tiles;
   out[2] = pl.grid;
   out[3] = pl.stages;
-  for (int g = 0; g < G; ++g) out[4 + g] = pl.splits[g];
+  out[4] = pl.sched.dp_tiles;
+  out[5] = pl.sched.total_tiles - pl.sched.dp_tiles;
+  out[6] = pl.sched.sk_iters > 0x7FFFFFFF ? 0x7FFFFFFF : static_cast<int>(pl.sched.sk_iters);
+  out[7] = pl.sched.sk_max_segs;
   return ok();
+}
+
+int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K, const int* L, int num_sms,
+                              int cta, int* out, int out_cap) {
+  int rc = check_shapes(G, M, N, K, L);
+  if (rc != NVFP4_OK) return rc;
+  if (num_sms < 1 || !out || out_cap < 0) return fail(NVFP4_ERR_INVALID_ARG, "bad schedule arguments");
+  Plan pl;
+  if ((rc = make_plan(G, M, N, K, L, num_sms, &pl)) != NVFP4_OK) return rc;
+  if (cta < 0 || cta >= pl.grid) return fail(NVFP4_ERR_INVALID_ARG, "cta %d outside the grid of %d", cta, pl.grid);
+  WorkCursor cur;
+  work_begin(pl.sched, cta, pl.grid, cur);
+  Work w;
+  int n = 0;
+  while (work_next(pl.sched, cta, pl.grid, cur, w)) {
+    if ((n + 1) * 9 <= out_cap) {
+      int* o = out + n * 9;
+      o[0] = w.g; o[1] = w.l; o[2] = w.tm; o[3] = w.tn; o[4] = w.kt0; o[5] = w.kt1;
+      o[6] = w.tile; o[7] = w.seg; o[8] = w.nseg;
+    }
+    ++n;
+  }
+  g_last_error.clear();
+  return n;
 }
 
 uint32_t nvfp4_gemm_encode_idesc(int M, int N) { return make_idesc_nvf4(M, N); }
@@ -491,10 +572,10 @@ uint64_t nvfp4_gemm_encode_smem_desc(uint32_t smem_addr, int swizzle128) {
 // library reserves until the process exits, and it calls no allocator.
 namespace {
 
-// Largest split-K partial area the static array holds: one wave of 128x128
-// fp32 partial tiles on a 160-SM device (the planner never puts more units
-// than SMs into a split launch).
-constexpr size_t kNoAllocPartialBytes = 160ull * kBM * 128 * sizeof(float);  // 10 MiB
+// Largest stream-K partial area the static array holds: 256 partial tiles of
+// 128 x 128 fp32 (16 MiB), e.g. the 56 tiles x 4 segments of a
+// 128 x 7168 x 16384 problem on 152 SMs.
+constexpr size_t kNoAllocPartialBytes = 256ull * kBM * 128 * sizeof(float);  // 16 MiB
 constexpr int kNoAllocCounters = 4096;       // output tiles of one split launch
 constexpr size_t kNoAllocHeader = 256;       // status word, padded
 constexpr size_t kNoAllocCounterBytes = kNoAllocCounters * sizeof(int);
@@ -557,13 +638,11 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
 
   Plan pl;
   if ((rc = make_plan(1, &M, &N, &K, &L, nd->sms, &pl)) != NVFP4_OK) return rc;
-  const bool split = pl.splits[0] > 1;
-  const size_t partial_bytes = split ? static_cast<size_t>(pl.total_units) * kBM * pl.bn * sizeof(float) : 0;
-  if (partial_bytes > kNoAllocPartialBytes || (split && pl.total_tiles > kNoAllocCounters))
+  if (pl.workspace_bytes > kNoAllocPartialBytes || pl.counters > kNoAllocCounters)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
-                "this problem needs %zu bytes of split-K scratch and %d tile counters; the static "
+                "this problem needs %zu bytes of stream-K scratch and %d tile counters; the static "
                 "no-allocation area holds %zu bytes and %d counters",
-                partial_bytes, pl.total_tiles, kNoAllocPartialBytes, kNoAllocCounters);
+                pl.workspace_bytes, pl.counters, kNoAllocPartialBytes, kNoAllocCounters);
 
   GemmParams p;
   memset(&p, 0, sizeof p);
@@ -574,20 +653,10 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   p.sfb[0] = static_cast<const uint8_t*>(SFB);
   p.M[0] = M;
   p.N[0] = N;
-  p.L[0] = L;
-  p.ktiles[0] = K / kBK;
-  p.tiles_m[0] = pl.tiles_m[0];
-  p.tiles_n[0] = pl.tiles_n[0];
-  p.splits[0] = pl.splits[0];
   p.sf_rows_a[0] = static_cast<int>(cdiv(M, 128));
   p.sf_rows_b[0] = static_cast<int>(cdiv(N, 128));
   p.a_streams[0] = M > N ? 1 : 0;
-  p.unit_start[0] = pl.unit_start[0];
-  p.unit_start[1] = pl.unit_start[1];
-  p.tile_start[0] = pl.tile_start[0];
-  p.tile_start[1] = pl.tile_start[1];
-  p.num_groups = 1;
-  p.total_units = pl.total_units;
+  p.sched = pl.sched;
   p.timeout_ns = g_timeout_ns.load();
   p.debug_skip_ktile = -1;
   p.status = reinterpret_cast<int*>(nd->scratch);
@@ -597,10 +666,10 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   // The array keeps whatever the previous call left: the status word and the
   // counters this launch uses must start at zero (the partial tiles are always
   // written before they are read).
-  const size_t clear = kNoAllocHeader + (split ? static_cast<size_t>(pl.total_tiles) * sizeof(int) : 0);
+  const size_t clear = kNoAllocHeader + static_cast<size_t>(pl.counters) * sizeof(int);
   if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
-  e = gemm_launch(pl.bn, p, pl.grid, stream);
+  e = gemm_launch(pl.bn, p, pl.grid, stream, false);  // follows a memset: plain launch
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }

@@ -196,6 +196,35 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
 }
 
 
+
+// ---------------------------------------------------------------- misc
+// Programmatic dependent launch (no-ops when the launch did not opt in).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+
+// L2 prefetches (no shared-memory destination, no completion tracking).  L2
+// is the coherence point for global memory, so a prefetch issued before a
+// preceding kernel finished writing the same bytes only costs bandwidth: the
+// real loads, issued after griddepcontrol.wait, see the final values.
+__device__ __forceinline__ void prefetch_tile_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Invalidate one 128-byte L2 line without writing it back (its contents
+// become undefined).  `p` must be 128-byte aligned.
+__device__ __forceinline__ void discard_l2(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------- warp-issued forms
 // The whole warp executes these with warp-uniform operands; elect.sync picks
 // one lane (the same lowest lane every time for a full warp) to issue.  Keeping

@@ -143,14 +143,28 @@ NVFP4_API int nvfp4_gemm_set_wait_timeout_ns(uint64_t ns);
 NVFP4_API int nvfp4_gemm_debug_inject_skip(int ktile);
 
 /*
- * Launch plan, host only (no GPU needed): what nvfp4_gemm_run_grouped would
- * launch for these sizes on a device with `num_sms` SMs.
- *   out[0] tile width BN along N       out[1] total work units
- *   out[2] grid size (CTAs)            out[3] pipeline stages
- *   out[4 + g] split-K factor of group g (g < G)
+ * Launch plan, host only (no GPU needed): how nvfp4_gemm_run_grouped would
+ * decompose these sizes on a device with `num_sms` SMs.  Output tiles are
+ * 128 x BN.  Tiles [0, dp_tiles) run whole, one per CTA per wave; the rest are
+ * cut into equal contiguous k-tile ranges, one per CTA ("stream-K"), and a
+ * tile covered by several CTAs is summed from their partial results in k
+ * order.  out_len >= 8:
+ *   out[0] BN            out[1] output tiles     out[2] grid (CTAs)
+ *   out[3] smem stages   out[4] dp_tiles         out[5] stream-K tiles
+ *   out[6] stream-K k-tile iterations            out[7] most CTAs sharing a tile
  */
 NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L,
                     int num_sms, int* out, int out_len);
+
+/*
+ * The work list CTA `cta` of that plan processes, host only, for checking the
+ * decomposition without a GPU.  Writes 9 ints per item while they fit in
+ * out_cap ints -- group, l, m-tile, n-tile, first k-tile, end k-tile, global
+ * tile index, segment index, segments of the tile -- and returns the number of
+ * items (or a negative status).
+ */
+NVFP4_API int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K,
+                                        const int* L, int num_sms, int cta, int* out, int out_cap);
 
 /*
  * nvfp4_gemm_run without any device allocation.  The source pages have no
@@ -161,7 +175,7 @@ NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, c
  * workspace on first use.
  *
  * Same arguments, layouts, shape contract and result as nvfp4_gemm_run (one
- * problem).  Split-K scratch (fp32 partial tiles, per-tile arrival counters,
+ * problem).  Stream-K scratch (fp32 partial tiles, per-tile arrival counters,
  * a status word) lives in one static device array of 10 MiB + 16.25 KiB that
  * every device which loads this library holds until the process exits.  The
  * first call on a device (with that device current) looks up the array's
@@ -171,7 +185,7 @@ NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, c
  *
  * All calls share the one array: calls whose work may overlap on the GPU
  * (different streams, or different host threads) race on it and give wrong
- * results; order them on one stream.  A problem whose split-K plan needs more
+ * results; order them on one stream.  A problem whose stream-K plan needs more
  * than the array holds returns NVFP4_ERR_UNSUPPORTED_SHAPE with the sizes in
  * the error string.  A bounded device wait that runs out ends the kernel early
  * and leaves C undefined; in this variant the timeout is recorded only in the

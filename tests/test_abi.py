@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = binding.header_functions()
-    assert len(names) == 12
+    assert len(names) == 13
     for n in names:
         assert hasattr(lib, n), n
         ctypes.cast(getattr(lib, n), ctypes.c_void_p)
@@ -55,28 +55,99 @@ def test_repacked_bytes(lib):
 
 def test_plan_single_tile_and_full_machine(lib):
     p = binding.nvfp4_gemm_plan([128], [128], [256], [1], 152)
-    assert p["bn"] == 128 and p["units"] == 1 and p["grid"] == 1 and p["splits"] == [1]
-    assert p["stages"] >= 4
+    assert p["bn"] == 128 and p["tiles"] == 1 and p["grid"] == 1
+    assert p["stages"] >= 4 and p["sk_max_segs"] == 1
     p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
-    assert p["splits"] == [1] and p["units"] == 4096 and p["grid"] == 152
+    # 4096 tiles = 26 full waves + 144: the last wave is nearly full, all data-parallel
+    assert p["tiles"] == 4096 and p["dp_tiles"] == 4096 and p["grid"] == 152 and p["sk_tiles"] == 0
 
 
-def test_plan_splits_skinny_problem(lib):
+def test_plan_stream_k_for_skinny_problem(lib):
     p = binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)
-    s = p["splits"][0]
-    assert s == 2 and p["units"] == 112 and p["grid"] == 112    # one wave of units
+    assert p["tiles"] == 56 and p["dp_tiles"] == 0 and p["sk_tiles"] == 56
+    assert p["grid"] == 112 and p["sk_iters"] == 56 * 64    # two equal segments per tile
+    assert p["sk_max_segs"] == 2
     p = binding.nvfp4_gemm_plan([128], [512], [4096], [1], 152)
-    assert p["splits"] == [4]                                    # capped: >= 4 k-tiles per unit
-    p = binding.nvfp4_gemm_plan([128], [128], [256], [1], 152)
-    assert p["splits"] == [1]
+    assert p["grid"] == 16 and p["sk_max_segs"] == 4         # capped: >= 4 k-tiles per CTA
 
 
-def test_plan_grouped(lib):
-    p = binding.nvfp4_gemm_plan([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], 152)
-    assert p["splits"] == [1, 1] and p["units"] == 8 * 32 + 16 * 56
+def test_plan_data_parallel_from_one_wave(lib):
     Ms = [384, 64, 1024, 256, 192, 512, 128, 768]
     p = binding.nvfp4_gemm_plan(Ms, [4096] * 8, [7168] * 8, [1] * 8, 152)
-    assert p["units"] == sum(-(-m // 128) for m in Ms) * 32
+    tiles = sum(-(-m // 128) for m in Ms) * 32
+    assert p["tiles"] == tiles == 864 and p["dp_tiles"] == 864 and p["sk_tiles"] == 0
+    p = binding.nvfp4_gemm_plan([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], 152)
+    assert p["tiles"] == 8 * 32 + 16 * 56 == p["dp_tiles"]
+
+
+SCHED_CASES = [
+    ([128], [7168], [16384], [1]),
+    ([128], [128], [256], [1]),
+    ([64], [2048], [4096], [1]),
+    ([300], [264], [1024], [2]),
+    ([384, 64, 1024, 256, 192, 512, 128, 768], [4096] * 8, [7168] * 8, [1] * 8),
+    ([1024, 2048], [4096, 7168], [7168, 2048], [1, 1]),
+    ([128, 256, 64], [1024, 512, 256], [4096, 1024, 8192], [1, 2, 1]),
+]
+
+
+def _check_schedule(M, N, K, L, sms):
+    plan = binding.nvfp4_gemm_plan(M, N, K, L, sms)
+    cover = {}
+    segs = {}
+    sk_lengths = []
+    for cta in range(plan["grid"]):
+        items = binding.nvfp4_gemm_debug_schedule(M, N, K, L, sms, cta)
+        sk = 0
+        for w in items:
+            g = w["g"]
+            tiles_m, tiles_n, kt = -(-M[g] // 128), -(-N[g] // plan["bn"]), K[g] // 256
+            assert 0 <= w["tm"] < tiles_m and 0 <= w["tn"] < tiles_n and 0 <= w["l"] < L[g]
+            assert 0 <= w["kt0"] < w["kt1"] <= kt
+            key = (g, w["l"], w["tm"], w["tn"])
+            for k in range(w["kt0"], w["kt1"]):
+                assert (key, k) not in cover, "k-tile covered twice"
+                cover[(key, k)] = cta
+            segs.setdefault(w["tile"], []).append((w["seg"], w["nseg"], w["kt0"], w["kt1"], key))
+            if w["tile"] >= plan["dp_tiles"]:
+                sk += w["kt1"] - w["kt0"]
+        sk_lengths.append(sk)
+    # every k-tile of every tile exactly once
+    total = sum(-(-M[g] // 128) * -(-N[g] // plan["bn"]) * L[g] * (K[g] // 256) for g in range(len(M)))
+    assert len(cover) == total
+    # segments of a tile: indices 0..n-1, consistent count, in k order, same coordinates
+    assert len(segs) == plan["tiles"]
+    for t, lst in segs.items():
+        lst.sort()
+        n = lst[0][1]
+        assert [x[0] for x in lst] == list(range(n)) and all(x[1] == n for x in lst)
+        assert n <= plan["sk_max_segs"] and len({x[4] for x in lst}) == 1
+        assert lst[0][2] == 0 and all(lst[i][3] == lst[i + 1][2] for i in range(n - 1))
+        if t < plan["dp_tiles"]:
+            assert n == 1
+    # stream-K ranges are equal to within one k-tile
+    if plan["sk_tiles"]:
+        assert max(sk_lengths) - min(sk_lengths) <= 1
+
+
+@pytest.mark.parametrize("case", range(len(SCHED_CASES)))
+def test_schedule_covers_every_k_tile_once(lib, case):
+    _check_schedule(*SCHED_CASES[case], 152)
+
+
+@pytest.mark.parametrize("mode", ["dp", "sk"])
+def test_schedule_forced_modes(lib, mode, monkeypatch):
+    monkeypatch.setenv("NVFP4_SCHEDULE", mode)
+    for case in (SCHED_CASES[0], SCHED_CASES[3], SCHED_CASES[5]):
+        _check_schedule(*case, 152)
+        p = binding.nvfp4_gemm_plan(*case, 152)
+        assert (p["sk_tiles"] == 0) if mode == "dp" else (p["dp_tiles"] == 0)
+
+
+def test_schedule_other_machine_sizes(lib):
+    for sms in (1, 7, 148, 160):
+        _check_schedule([128], [7168], [16384], [1], sms)
+        _check_schedule([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], sms)
 
 
 @pytest.mark.parametrize("M,N,K,L,code", [

@@ -71,11 +71,11 @@ def test_one_hot_scales_pin_the_atom_layout():
         assert_close_full(C, p)
 
 
-def test_split_k_is_deterministic():
+def test_stream_k_is_deterministic():
     binding = require_gpu()
     p = workloads.make_random_problem(11, 128, 2048, 8192)
     plan = binding.nvfp4_gemm_plan([128], [2048], [8192], [1], torch.cuda.get_device_properties(0).multi_processor_count)
-    assert plan["splits"][0] > 1
+    assert plan["sk_max_segs"] > 1
     d = to_device(p)
     outs = []
     for _ in range(3):
@@ -89,27 +89,35 @@ def test_split_k_is_deterministic():
     assert_close_full(outs[0], p)
 
 
-def test_grouped_small_equals_oracle_and_singles():
-    binding = require_gpu()
-    shapes = [(128, 256, 512, 1), (64, 136, 256, 1), (300, 128, 1024, 2), (128, 1024, 4096, 1)]
-    probs = [workloads.make_random_problem(200 + i, *s) for i, s in enumerate(shapes)]
-    devs = [to_device(p) for p in probs]
-    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+def _grouped(binding, devs, probs, Cs):
     binding.nvfp4_gemm_run_grouped(
         len(probs), [d["A"] for d in devs], [d["B"] for d in devs], [d["SFA"] for d in devs],
         [d["SFB"] for d in devs], [c for _, c in Cs], [p["M"] for p in probs], [p["N"] for p in probs],
         [p["K"] for p in probs], [p["L"] for p in probs])
     binding.nvfp4_gemm_check_device_status()
+
+
+def test_grouped_small_equals_oracle_and_singles(monkeypatch):
+    binding = require_gpu()
+    shapes = [(128, 256, 512, 1), (64, 136, 256, 1), (300, 128, 1024, 2), (128, 1024, 4096, 1)]
+    probs = [workloads.make_random_problem(200 + i, *s) for i, s in enumerate(shapes)]
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    _grouped(binding, devs, probs, Cs)
     refs = oracle.gemm_grouped(probs)
-    for p, d, (buf, c), ref in zip(probs, devs, Cs, refs):
+    for p, (buf, c), ref in zip(probs, Cs, refs):
         check_canary(buf, p["M"], p["N"], p["L"])
         assert_close_full(c, p)
-        # grouped launch == single launch of the same problem, bit for bit
+    # With whole-tile (data-parallel) decomposition every tile is summed in
+    # k order by one CTA, so the grouped launch equals single launches bit for bit.
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    Cg = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    _grouped(binding, devs, probs, Cg)
+    for p, d, (_, c) in zip(probs, devs, Cg):
         _, c1 = alloc_c(p["M"], p["N"], p["L"])
         run_single(d, c1)
         torch.cuda.synchronize()
-        if binding.nvfp4_gemm_plan([p["M"]], [p["N"]], [p["K"]], [p["L"]], 152)["splits"] == [1]:
-            assert torch.equal(c.view(torch.int16), c1.view(torch.int16))
+        assert torch.equal(c.view(torch.int16), c1.view(torch.int16))
 
 
 def _run_workload(name):
@@ -142,3 +150,36 @@ def test_skinny_workload_whole_output():
     """The bench workload compared on every output element."""
     probs, Cs = _run_workload("skinny_128x7168x16384")
     assert_close_full(Cs[0][1], probs[0])
+
+
+@pytest.mark.parametrize("mode", ["dp", "sk"])
+@pytest.mark.parametrize("M,N,K,L", [(256, 512, 2048, 1), (200, 136, 1024, 2), (128, 7168, 4096, 1)])
+def test_parity_forced_schedules(mode, M, N, K, L, monkeypatch):
+    """The same problem decomposed data-parallel and fully stream-K."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_SCHEDULE", mode)
+    p = workloads.make_random_problem(M + N + K + (mode == "sk"), M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
+
+
+def test_parity_grouped_stream_k_across_groups(monkeypatch):
+    """Stream-K ranges that cross group boundaries (groups with different K)."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_SCHEDULE", "sk")
+    shapes = [(128, 1024, 4096, 1), (256, 512, 1024, 2), (64, 256, 8192, 1)]
+    probs = [workloads.make_random_problem(300 + i, *s) for i, s in enumerate(shapes)]
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    binding.nvfp4_gemm_run_grouped(
+        len(probs), [d["A"] for d in devs], [d["B"] for d in devs], [d["SFA"] for d in devs],
+        [d["SFB"] for d in devs], [c for _, c in Cs], [p["M"] for p in probs], [p["N"] for p in probs],
+        [p["K"] for p in probs], [p["L"] for p in probs])
+    binding.nvfp4_gemm_check_device_status()
+    for p, (buf, c) in zip(probs, Cs):
+        check_canary(buf, p["M"], p["N"], p["L"])
+        assert_close_full(c, p)

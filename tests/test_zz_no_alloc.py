@@ -44,11 +44,11 @@ def _check_against_existing(p, ref, got):
 def test_noalloc_matches_existing_entry_point_call_after_call():
     binding = require_gpu()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # split-K problems, so the static scratch (partials + counters) is used
+    # stream-K problems, so the static scratch (partials + counters) is used
     shapes = [(128, 7168, 16384, 1), (256, 2048, 4096, 1), (128, 7168, 16384, 1)]
     for i, shape in enumerate(shapes):
         plan = binding.nvfp4_gemm_plan([shape[0]], [shape[1]], [shape[2]], [shape[3]], sms)
-        assert plan["splits"][0] > 1
+        assert plan["sk_max_segs"] > 1
         p = workloads.make_random_problem(900 + i, *shape)
         ref, got = _both(binding, p)
         _check_against_existing(p, ref, got)
@@ -56,14 +56,15 @@ def test_noalloc_matches_existing_entry_point_call_after_call():
 
 def test_noalloc_rejects_plans_beyond_the_static_area():
     binding = require_gpu()
-    p = workloads.make_random_problem(7, 128, 7168, 16384)
+    p = workloads.make_random_problem(7, 2048, 2048, 2048)
     d = to_device(p)
-    _, C = alloc_c(128, 7168, 1)
-    os.environ["NVFP4_SPLIT_K"] = "16"      # 896 partial tiles: more than the area holds
+    _, C = alloc_c(2048, 2048, 1)
+    # all 256 tiles as stream-K, two segments each: 32 MiB of partials
+    os.environ["NVFP4_SCHEDULE"] = "sk"
     try:
         with pytest.raises(binding.Nvfp4Error) as e:
-            binding.nvfp4_gemm_run_noalloc(d["A"], d["B"], d["SFA"], d["SFB"], C, 128, 7168, 16384, 1)
+            binding.nvfp4_gemm_run_noalloc(d["A"], d["B"], d["SFA"], d["SFB"], C, 2048, 2048, 2048, 1)
         assert e.value.code == -2
         assert "static" in str(e.value)
     finally:
-        del os.environ["NVFP4_SPLIT_K"]
+        del os.environ["NVFP4_SCHEDULE"]
