@@ -532,6 +532,7 @@ static cudaError_t prepare_bn() {
 cudaError_t gemm_prepare_device(int bn) {
   switch (bn) {
     case 128: return prepare_bn<128>();
+    case 256: return prepare_bn<256>();
     default: return cudaErrorInvalidValue;
   }
 }
@@ -539,6 +540,7 @@ cudaError_t gemm_prepare_device(int bn) {
 cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   switch (bn) {
     case 128: return launch_bn<128>(p, grid, stream, pdl);
+    case 256: return launch_bn<256>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -68,7 +68,7 @@ struct DeviceState {
   int sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;       // device status word
-  bool prepared_bn128 = false;
+  bool prepared_bn[2] = {false, false};  // BN = 128, 256
 };
 
 struct Workspace {
@@ -236,8 +236,24 @@ SchedMode sched_mode() {
 // NVFP4_SCHEDULE=sk forces stream-K over all tiles with one CTA per SM.
 constexpr int kMinSkIters = 4;
 
+// Tile width along N (NVFP4_BN = 128 | 256 overrides).  128 x 256 tiles need
+// half the MMA and scale-copy instructions per FLOP and re-read A half as
+// often, so they win whenever they still give every SM a whole tile
+// (GB300: 8192^3 3803 -> 4482 TFLOP/s, MoE 8 groups 61.8 -> 54.8 us); below
+// that the stream-K path with 128-wide tiles is faster (128 x 7168 x 16384:
+// 22.7 vs 28.8 us).
+int choose_bn(int G, const int* M, const int* N, const int* L, int sms) {
+  if (const char* env = getenv("NVFP4_BN")) {
+    const int v = atoi(env);
+    if (v == 128 || v == 256) return v;
+  }
+  long long tiles256 = 0;
+  for (int g = 0; g < G; ++g) tiles256 += cdiv(M[g], kBM) * cdiv(N[g], 256) * L[g];
+  return tiles256 >= sms ? 256 : 128;
+}
+
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl) {
-  pl->bn = 128;
+  pl->bn = choose_bn(G, M, N, L, sms);
   pl->stages = gemm_stages(pl->bn);
   Schedule& s = pl->sched;
   memset(&s, 0, sizeof s);
@@ -422,9 +438,10 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
 
   Plan pl;
   if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
-  if (pl.bn == 128 && !ds->prepared_bn128) {
-    if ((e = gemm_prepare_device(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    ds->prepared_bn128 = true;
+  const int bn_i = pl.bn == 256 ? 1 : 0;
+  if (!ds->prepared_bn[bn_i]) {
+    if ((e = gemm_prepare_device(pl.bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    ds->prepared_bn[bn_i] = true;
   }
 
   GemmParams p;
@@ -611,6 +628,7 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
     if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
     if ((e = gemm_prepare_device(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    if ((e = gemm_prepare_device(256)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     d.scratch = static_cast<unsigned char*>(ptr);
     d.ready = true;
   }

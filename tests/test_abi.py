@@ -58,8 +58,8 @@ def test_plan_single_tile_and_full_machine(lib):
     assert p["bn"] == 128 and p["tiles"] == 1 and p["grid"] == 1
     assert p["stages"] >= 4 and p["sk_max_segs"] == 1
     p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
-    # 4096 tiles = 26 full waves + 144: the last wave is nearly full, all data-parallel
-    assert p["tiles"] == 4096 and p["dp_tiles"] == 4096 and p["grid"] == 152 and p["sk_tiles"] == 0
+    # 128 x 256 tiles: 2048 of them, all data-parallel
+    assert p["bn"] == 256 and p["tiles"] == 2048 and p["dp_tiles"] == 2048 and p["grid"] == 152
 
 
 def test_plan_stream_k_for_skinny_problem(lib):
@@ -74,10 +74,10 @@ def test_plan_stream_k_for_skinny_problem(lib):
 def test_plan_data_parallel_from_one_wave(lib):
     Ms = [384, 64, 1024, 256, 192, 512, 128, 768]
     p = binding.nvfp4_gemm_plan(Ms, [4096] * 8, [7168] * 8, [1] * 8, 152)
-    tiles = sum(-(-m // 128) for m in Ms) * 32
-    assert p["tiles"] == tiles == 864 and p["dp_tiles"] == 864 and p["sk_tiles"] == 0
+    tiles = sum(-(-m // 128) for m in Ms) * 16
+    assert p["bn"] == 256 and p["tiles"] == tiles == 432 and p["dp_tiles"] == 432 and p["sk_tiles"] == 0
     p = binding.nvfp4_gemm_plan([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], 152)
-    assert p["tiles"] == 8 * 32 + 16 * 56 == p["dp_tiles"]
+    assert p["bn"] == 256 and p["tiles"] == 8 * 16 + 16 * 28 == p["dp_tiles"]
 
 
 SCHED_CASES = [

@@ -183,3 +183,20 @@ def test_parity_grouped_stream_k_across_groups(monkeypatch):
     for p, (buf, c) in zip(probs, Cs):
         check_canary(buf, p["M"], p["N"], p["L"])
         assert_close_full(c, p)
+
+
+@pytest.mark.parametrize("mode", ["auto", "sk"])
+@pytest.mark.parametrize("M,N,K,L", [(256, 512, 2048, 1), (200, 136, 1024, 2), (129, 264, 512, 1),
+                                     (128, 7168, 4096, 1), (384, 1024, 1024, 1)])
+def test_parity_wide_tiles(mode, M, N, K, L, monkeypatch):
+    """128 x 256 output tiles (two scale atoms per B k-tile, one accumulator)."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", "256")
+    monkeypatch.setenv("NVFP4_SCHEDULE", mode)
+    p = workloads.make_random_problem(M + 3 * N + K, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
