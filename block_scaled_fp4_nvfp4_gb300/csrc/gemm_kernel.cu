@@ -108,9 +108,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 }  // namespace
 
-template <int BN>
+template <int BN, int CL>
 __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = TileCfg<BN>;
+  static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
+  // CL == 2: the two CTAs of a cluster run tiles with the same B columns;
+  // each loads half of every B tile and of the B scale slabs and multicasts
+  // it to both, halving B's L2 -> SM traffic.
+  constexpr uint16_t kPeers = static_cast<uint16_t>((1u << CL) - 1u);
+  constexpr int kBHalfRows = BN / CL;
   constexpr int kStages = Cfg::kStages;
   static_assert(kStages <= kMaxStages, "stage ring too deep");
 
@@ -123,6 +129,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int crank = CL > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
+  const int unit = static_cast<int>(blockIdx.x) / CL;   // cluster index
+  const int units = static_cast<int>(gridDim.x) / CL;   // clusters in the grid
 
   auto full_bar = [&](int s) { return ptx::smem_addr(&ctl.full[s]); };
   auto empty_bar = [&](int s) { return ptx::smem_addr(&ctl.empty[s]); };
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), CL);  // released by the MMAs of every CTA that reads it
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full_bar(b), 1);
@@ -152,12 +161,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       ptx::prefetch_tensormap(&p.tmC[g]);
     }
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), Cfg::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
+  if constexpr (CL > 1) ptx::cluster_sync();  // peers' barriers exist before any multicast
   ptx::tc_fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
 
@@ -168,17 +178,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   // comes after the wait.
   if (warp == 0 && lane == 0 && p.prefetch_ktiles > 0) {
     WorkCursor pc;
-    work_begin(p.sched, blockIdx.x, gridDim.x, pc);
+    work_begin(p.sched, unit, units, pc, crank);
     Work pw;
     int left = p.prefetch_ktiles;
-    while (left > 0 && work_next(p.sched, blockIdx.x, gridDim.x, pc, pw)) {
+    while (left > 0 && work_next(p.sched, unit, units, pc, pw)) {
       const size_t atoms = static_cast<size_t>(p.sched.ktiles[pw.g]) * 4;
       const uint8_t* sfa = p.sfa[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_a[pw.g] + pw.tm) * atoms * kSfAtomBytes;
       const int sfb_block0 = pw.tn * Cfg::kSfbBlocks;
       const uint8_t* sfb = p.sfb[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_b[pw.g] + sfb_block0) * atoms * kSfAtomBytes;
       for (int kt = pw.kt0; kt < pw.kt1 && left > 0; ++kt, --left) {
         ptx::prefetch_tile_l2_3d(&p.tmA[pw.g], kt * kBKBytes, pw.tm * kBM, pw.l);
-        ptx::prefetch_tile_l2_3d(&p.tmB[pw.g], kt * kBKBytes, pw.tn * BN, pw.l);
+        ptx::prefetch_tile_l2_3d(&p.tmB[pw.g], kt * kBKBytes, pw.tn * BN + crank * kBHalfRows, pw.l);
         ptx::prefetch_l2(sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
         if (sfb_block0 < p.sf_rows_b[pw.g]) ptx::prefetch_l2(sfb + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
       }
@@ -189,10 +199,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   const Waiter W{&ctl.abort, p.status, p.timeout_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // The whole warp runs the loop with warp-uniform values; one elected lane
-    // issues each copy (see the *_elect wrappers).
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    // Two producer warps fill every stage together: warp 0 arms the stage's
+    // barrier with the whole byte count and loads A and its scales, warp 1
+    // loads B and its scales.  Splitting the copies halves the time from a
+    // stage's release to its refill, which bounds the ring's throughput (the
+    // barrier's byte count may briefly go negative when warp 1's bytes land
+    // first; the phase still needs warp 0's arrival).  Within a warp every lane
+    // runs the loop with warp-uniform values and one elected lane issues each
+    // copy (see the *_elect wrappers).
     const uint64_t pol_stream = ptx::policy_evict_first();
     const uint64_t pol_keep = ptx::policy_evict_last();
     int stage = 0;
@@ -203,9 +219,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int count = 0;
     bool ok = true;
     WorkCursor cur;
-    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    work_begin(p.sched, unit, units, cur, crank);
     Work x;
-    while (ok && work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
+    while (ok && work_next(p.sched, unit, units, cur, x)) {
       const CUtensorMap* mapA = &p.tmA[x.g];
       const CUtensorMap* mapB = &p.tmB[x.g];
       const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
@@ -233,14 +249,25 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           armed[stage] = -1;  // test-only: nothing issued, nothing in flight
         } else {
           const uint32_t fb = full_bar(stage);
-          ptx::mbar_arrive_expect_tx_elect(fb, stage_tx);
-          ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
-          ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
-          ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
-          for (int j = 0; j < nsfb; ++j)
-            ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
-                                 sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
-                                 kSfSlabBytes, fb, polB);
+          if (warp == 0) {
+            ptx::mbar_arrive_expect_tx_elect(fb, stage_tx);
+            ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
+            ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
+          } else if constexpr (CL == 1) {
+            ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
+            for (int j = 0; j < nsfb; ++j)
+              ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
+                                   sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
+                                   kSfSlabBytes, fb, polB);
+          } else {
+            // this CTA's half of the B rows and every CL-th scale slab, for both CTAs
+            ptx::tma_load_3d_mc_elect(sB + crank * kBHalfRows * kBKBytes, mapB, kt * kBKBytes,
+                                      x.tn * BN + crank * kBHalfRows, x.l, fb, polB, kPeers);
+            for (int j = crank; j < nsfb; j += CL)
+              ptx::bulk_load_mc_elect(sSFB + j * kSfSlabBytes,
+                                      sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
+                                      kSfSlabBytes, fb, polB, kPeers);
+          }
           armed[stage] = static_cast<int>(phase);
         }
         ++count;
@@ -259,7 +286,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       }
       __syncwarp();
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // Whole warp in the loop, one elected lane issues every tcgen05 operation
     // (always the same lane, so its commits track all of them).
@@ -270,9 +297,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     uint32_t aphase = 0;
     bool ok = true;
     WorkCursor cur;
-    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    work_begin(p.sched, unit, units, cur, crank);
     Work x;
-    while (ok && work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
+    while (ok && work_next(p.sched, unit, units, cur, x)) {
       if (!warp_wait(W, acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
         ok = false;
         break;
@@ -312,7 +339,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
                                  sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
                                  (kt > x.kt0 || kb > 0) ? 1u : 0u);
         }
-        ptx::tc_commit_elect(empty_bar(stage));
+        if constexpr (CL == 1)
+          ptx::tc_commit_elect(empty_bar(stage));
+        else
+          ptx::tc_commit_mc_elect(empty_bar(stage), kPeers);  // the stage is free once both CTAs read it
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -333,7 +363,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;           // epilogue warp 0..3
+    const int ew = warp - kFirstEpiWarp;  // epilogue warp 0..3
     const int sub = warp & 3;          // tensor-memory sub-partition this warp may read
     const int row = sub * 32 + lane;   // tile row owned by this thread
     const uint32_t gather_bar = ptx::smem_addr(&ctl.epi_gather);
@@ -341,27 +371,32 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t gphase = 0;
-    int buf = 0;
     // Convert 64 fp32 columns of this thread's row to fp16, stage them as one
     // 128-byte swizzled row of a 32 x 64 box and let lane 0 store the box.
-    auto store_chunk = [&](const Work& x, int q, const float* v) {
-      const uint32_t sbuf = epi_base + (ew * 2 + buf) * Cfg::kEpiBufBytes;
-      if (lane == 0) ptx::bulk_wait_read<1>();  // the store that last read this buffer is done
+    // Store 32 columns of this warp's 32 rows, packed as 16 half2 words per
+    // thread: 64-byte-swizzled staging (16-byte chunk j of row r at chunk
+    // j ^ ((r >> 1) & 3), conflict-free) and one TMA store of the 32 x 32 box.
+    auto store_box = [&](const Work& x, int col, const uint32_t* h) {
+      const uint32_t sbuf = epi_base + ew * Cfg::kEpiBufBytes;
+      if (lane == 0) ptx::bulk_wait_read<0>();  // the previous store has read the buffer
       __syncwarp();
-      const uint32_t row_addr = sbuf + lane * 128;
+      const uint32_t row_addr = sbuf + lane * 64;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float* f = v + 8 * j;
-        st_shared_v4(row_addr + ((j ^ (lane & 7)) << 4), pack_half2(f[0], f[1]), pack_half2(f[2], f[3]),
-                     pack_half2(f[4], f[5]), pack_half2(f[6], f[7]));
-      }
+      for (int j = 0; j < 4; ++j)
+        st_shared_v4(row_addr + ((j ^ ((lane >> 1) & 3)) << 4), h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        ptx::tma_store_3d(&p.tmC[x.g], sbuf, x.tn * BN + 64 * q, x.tm * kBM + sub * 32, x.l);
+        ptx::tma_store_3d(&p.tmC[x.g], sbuf, x.tn * BN + col, x.tm * kBM + sub * 32, x.l);
         ptx::bulk_commit();
       }
-      buf ^= 1;
+    };
+    auto store_chunk = [&](const Work& x, int q, const float* v) {
+      uint32_t h[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+      store_box(x, 64 * q, h);
+      store_box(x, 64 * q + 32, h + 16);
     };
     // Tensor memory -> registers, 64 columns of this thread's row.
     auto load_chunk = [&](uint32_t t_addr, float* v) {
@@ -376,9 +411,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     };
 
     WorkCursor cur;
-    work_begin(p.sched, blockIdx.x, gridDim.x, cur);
+    work_begin(p.sched, unit, units, cur, crank);
     Work x;
-    while (work_next(p.sched, blockIdx.x, gridDim.x, cur, x)) {
+    while (work_next(p.sched, unit, units, cur, x)) {
       if (!warp_wait(W, acc_full_bar(ab), aphase, kStatusTimeoutEpilogue)) break;
       ptx::tc_fence_after_sync();
       const uint32_t t_row = tmem + (static_cast<uint32_t>(sub * 32) << 16) + ab * BN;
@@ -395,12 +430,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       };
 
       if (x.nseg == 1) {
-#pragma unroll 1
+        // Drain the whole accumulator row into registers as fp16 first and
+        // release it, so the next tile's MMAs start while this one is stored.
+        uint32_t h[BN / 2];
+#pragma unroll
         for (int q = 0; q < BN / 64; ++q) {
           float v[64];
           load_chunk(t_row + 64 * q, v);
-          if (q == BN / 64 - 1) release_acc();
-          if (rows_live) store_chunk(x, q, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h[32 * q + i] = pack_half2(v[2 * i], v[2 * i + 1]);
+        }
+        release_acc();
+        if (rows_live) {
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) store_box(x, 32 * c, &h[16 * c]);
         }
         continue;
       }
@@ -499,12 +542,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   ptx::tc_fence_before_sync();
   __syncthreads();
+  // No CTA leaves while its peer may still multicast into its shared memory
+  // or signal its barriers.
+  if constexpr (CL > 1) ptx::cluster_sync();
   ptx::tc_fence_after_sync();
-  if (warp == 1) ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
 // ---------------------------------------------------------------- launcher
-template <int BN>
+template <int BN, int CL>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
   using Cfg = TileCfg<BN>;
   cudaLaunchConfig_t cfg = {};
@@ -515,34 +561,81 @@ static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream,
   // Programmatic dependent launch: this grid may start while the previous
   // kernel on the stream finishes; the kernel waits for it (griddepcontrol)
   // before its first global-memory access.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (CL > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = CL;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN>, p);
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, CL>, p);
 }
 
-template <int BN>
+template <int BN, int CL>
 static cudaError_t prepare_bn() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               TileCfg<BN>::kDynSmem);
 }
 
+// Largest number of co-resident clusters of CL CTAs (0 on error).
+template <int BN, int CL>
+static int max_clusters_bn() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * 1024, 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = TileCfg<BN>::kDynSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<BN, CL>, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
 cudaError_t gemm_prepare_device(int bn) {
+  cudaError_t e;
   switch (bn) {
-    case 128: return prepare_bn<128>();
-    case 256: return prepare_bn<256>();
+    case 128:
+      if ((e = prepare_bn<128, 1>()) != cudaSuccess) return e;
+      return prepare_bn<128, 2>();
+    case 256:
+      if ((e = prepare_bn<256, 1>()) != cudaSuccess) return e;
+      return prepare_bn<256, 2>();
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
+cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
+  if (cluster == 2) {
+    switch (bn) {
+      case 128: return launch_bn<128, 2>(p, grid, stream, pdl);
+      case 256: return launch_bn<256, 2>(p, grid, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (bn) {
-    case 128: return launch_bn<128>(p, grid, stream, pdl);
-    case 256: return launch_bn<256>(p, grid, stream, pdl);
+    case 128: return launch_bn<128, 1>(p, grid, stream, pdl);
+    case 256: return launch_bn<256, 1>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int gemm_max_clusters(int bn, int cluster) {
+  if (cluster != 2) return 0;
+  return bn == 256 ? max_clusters_bn<256, 2>() : max_clusters_bn<128, 2>();
 }
 
 int gemm_stages(int bn) {

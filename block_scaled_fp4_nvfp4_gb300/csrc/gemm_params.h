@@ -23,8 +23,13 @@ constexpr int kMmaK = 64;                  // K of one kind::mxf4nvf4 MMA
 constexpr int kSfAtomBytes = 512;          // 128 rows x 4 scales
 constexpr int kSfSlabBytes = 4 * kSfAtomBytes;  // one 128-row block, one k-tile
 
-constexpr int kNumThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// Warp roles: kProducerWarps TMA producers, one MMA warp, four epilogue warps
+// (one per 32-lane tensor-memory sub-partition).
+constexpr int kProducerWarps = 2;  // warp 0: A + SFA, warp 1: B + SFB
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kFirstEpiWarp = kProducerWarps + 1;
 constexpr int kEpiWarps = 4;
+constexpr int kNumThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
 
 // Status codes a kernel may leave in the device status word.
 constexpr int kStatusTimeoutProducer = 1;
@@ -37,7 +42,7 @@ constexpr int kStatusTimeoutEpilogue = 3;
 struct GemmParams {
   CUtensorMap tmA[kMaxGroups];   // uint8 {K/2, M, L}, box {128, 128, 1}, 128B swizzle
   CUtensorMap tmB[kMaxGroups];   // uint8 {K/2, N, L}, box {128, BN, 1}, 128B swizzle
-  CUtensorMap tmC[kMaxGroups];   // fp16 {N, M, L}, box {64, 32, 1}, 128B swizzle
+  CUtensorMap tmC[kMaxGroups];   // fp16 {N, M, L}, box {32, 32, 1}, 64B swizzle
   const uint8_t* sfa[kMaxGroups];  // repacked scales
   const uint8_t* sfb[kMaxGroups];
   int M[kMaxGroups], N[kMaxGroups];
@@ -61,9 +66,13 @@ struct TileCfg {
   static constexpr int kBBytes = BN * kBKBytes;                // BN * 128 B
   static constexpr int kSfbBlocks = (BN + 127) / 128;          // 128-row scale blocks
   static constexpr int kStageBytes = kABytes + kBBytes + kSfSlabBytes + kSfbBlocks * kSfSlabBytes;
-  static constexpr int kEpiBufBytes = 32 * 128;                // 32 rows x 64 fp16
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
-  static constexpr int kSmemBudget = 227 * 1024;
+  // Epilogue staging: one 32 rows x 32 fp16 box (64-byte swizzle) per
+  // epilogue warp, so that shared memory goes to the operand ring instead
+  // (4 stages at BN = 256, 6 at BN = 128).
+  static constexpr int kEpiBoxCols = 32;
+  static constexpr int kEpiBufBytes = 32 * kEpiBoxCols * 2;     // 2 KB
+  static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
+  static constexpr int kSmemBudget = 227 * 1024 - 512;           // minus static shared memory
   static constexpr int kStages = (kSmemBudget - kEpiBytes - 1024) / kStageBytes;
   static constexpr int kDynSmem = kStages * kStageBytes + kEpiBytes + 1024;  // +1024 alignment slack
   // Tensor memory: accumulators first, then a ring of scale slots.

@@ -29,7 +29,8 @@
 
 namespace nvfp4 {
 cudaError_t gemm_prepare_device(int bn);
-cudaError_t gemm_launch(int bn, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
+int gemm_max_clusters(int bn, int cluster);
 int gemm_stages(int bn);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
 }  // namespace nvfp4
@@ -69,6 +70,7 @@ struct DeviceState {
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;       // device status word
   bool prepared_bn[2] = {false, false};  // BN = 128, 256
+  int max_clusters[2] = {0, 0};          // co-resident 2-CTA clusters, BN = 128, 256
 };
 
 struct Workspace {
@@ -165,9 +167,9 @@ int encode_operand_map(CUtensorMap* out, const void* ptr, int rows, int K, int L
   return NVFP4_OK;
 }
 
-// fp16 C [L][M][N]; box: 64 columns x 32 rows.
+// fp16 C [L][M][N]; box: 32 columns x 32 rows, 64-byte swizzle.
 int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
-  MapKey key{1, reinterpret_cast<uintptr_t>(ptr), M, N, L, 32};
+  MapKey key{2, reinterpret_cast<uintptr_t>(ptr), M, N, L, 32};
   auto it = g_maps.find(key);
   if (it != g_maps.end()) {
     *out = it->second;
@@ -177,10 +179,10 @@ int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
   if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(L)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N) * 2 * M};
-  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t box[3] = {32, 32, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled(C M=%d N=%d L=%d) failed: %d", M, N, L,
@@ -193,8 +195,9 @@ int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
 // ------------------------------------------------------------------ planning
 struct Plan {
   int bn = 128;
+  int cluster = 1;  // CTAs per cluster (2: pairs sharing B tiles by multicast)
   int stages = 0;
-  int grid = 0;
+  int grid = 0;     // CTAs
   int tiles_m[kMaxGroups] = {}, tiles_n[kMaxGroups] = {};
   Schedule sched = {};
   size_t workspace_bytes = 0;  // stream-K partials
@@ -252,7 +255,24 @@ int choose_bn(int G, const int* M, const int* N, const int* L, int sms) {
   return tiles256 >= sms ? 256 : 128;
 }
 
-int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl) {
+// Clusters of two CTAs (tiles 2q, 2q+1 of the same B columns, B multicast)
+// halve the B tiles' L2 -> SM traffic.  Used for data-parallel plans whose
+// groups all have an even number of 128-row m-tiles and at least two waves of
+// tiles; NVFP4_CLUSTER = 1 | 2 overrides (2 only where the pairing is valid).
+int choose_cluster(const Schedule& s, int sms, bool allow) {
+  if (!allow || sms < 2 || s.dp_tiles != s.total_tiles) return 1;
+  for (int g = 0; g < s.num_groups; ++g)
+    if (s.tiles_m[g] % 2 != 0) return 1;
+  int want = s.total_tiles >= 2 * sms ? 2 : 1;
+  if (const char* env = getenv("NVFP4_CLUSTER")) {
+    const int v = atoi(env);
+    if (v == 1 || v == 2) want = v;
+  }
+  return want;
+}
+
+int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl,
+              bool allow_cluster = true) {
   pl->bn = choose_bn(G, M, N, L, sms);
   pl->stages = gemm_stages(pl->bn);
   Schedule& s = pl->sched;
@@ -336,6 +356,14 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     pl->workspace_bytes = 0;
   }
   if (pl->grid < 1) pl->grid = 1;
+  s.cluster = 1;
+  pl->cluster = choose_cluster(s, sms, allow_cluster);
+  if (pl->cluster > 1) {
+    s.cluster = pl->cluster;
+    const long long groups = tiles / pl->cluster;
+    const long long per_wave = sms / pl->cluster;
+    pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * pl->cluster);
+  }
   return NVFP4_OK;
 }
 
@@ -438,6 +466,19 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
 
   Plan pl;
   if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
+  if (pl.cluster > 1) {
+    // persistent grid: no more clusters than can be co-resident
+    const int bi = pl.bn == 256 ? 1 : 0;
+    if (ds->max_clusters[bi] == 0) ds->max_clusters[bi] = gemm_max_clusters(pl.bn, pl.cluster);
+    const int mc = ds->max_clusters[bi];
+    if (mc < 1) {
+      pl.cluster = 1;
+      pl.sched.cluster = 1;
+      pl.grid = pl.sched.total_tiles < ds->sms ? pl.sched.total_tiles : ds->sms;
+    } else if (pl.grid / pl.cluster > mc) {
+      pl.grid = mc * pl.cluster;
+    }
+  }
   const int bn_i = pl.bn == 256 ? 1 : 0;
   if (!ds->prepared_bn[bn_i]) {
     if ((e = gemm_prepare_device(pl.bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
@@ -448,7 +489,7 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
   memset(&p, 0, sizeof p);
   for (int g = 0; g < G; ++g) {
     if ((rc = encode_operand_map(&p.tmA[g], A[g], M[g], K[g], L[g], kBM)) != NVFP4_OK) return rc;
-    if ((rc = encode_operand_map(&p.tmB[g], B[g], N[g], K[g], L[g], pl.bn)) != NVFP4_OK) return rc;
+    if ((rc = encode_operand_map(&p.tmB[g], B[g], N[g], K[g], L[g], pl.bn / pl.cluster)) != NVFP4_OK) return rc;
     if ((rc = encode_c_map(&p.tmC[g], C[g], M[g], N[g], L[g])) != NVFP4_OK) return rc;
     p.sfa[g] = static_cast<const uint8_t*>(SFA[g]);
     p.sfb[g] = static_cast<const uint8_t*>(SFB[g]);
@@ -474,7 +515,7 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.counters = w->counters;
   }
 
-  e = gemm_launch(pl.bn, p, pl.grid, stream, true);
+  e = gemm_launch(pl.bn, pl.cluster, p, pl.grid, stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }
@@ -544,6 +585,7 @@ int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* 
   out[5] = pl.sched.total_tiles - pl.sched.dp_tiles;
   out[6] = pl.sched.sk_iters > 0x7FFFFFFF ? 0x7FFFFFFF : static_cast<int>(pl.sched.sk_iters);
   out[7] = pl.sched.sk_max_segs;
+  if (out_len >= 9) out[8] = pl.cluster;
   return ok();
 }
 
@@ -556,10 +598,11 @@ int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K, c
   if ((rc = make_plan(G, M, N, K, L, num_sms, &pl)) != NVFP4_OK) return rc;
   if (cta < 0 || cta >= pl.grid) return fail(NVFP4_ERR_INVALID_ARG, "cta %d outside the grid of %d", cta, pl.grid);
   WorkCursor cur;
-  work_begin(pl.sched, cta, pl.grid, cur);
+  const int unit = cta / pl.cluster, units = pl.grid / pl.cluster;
+  work_begin(pl.sched, unit, units, cur, cta % pl.cluster);
   Work w;
   int n = 0;
-  while (work_next(pl.sched, cta, pl.grid, cur, w)) {
+  while (work_next(pl.sched, unit, units, cur, w)) {
     if ((n + 1) * 9 <= out_cap) {
       int* o = out + n * 9;
       o[0] = w.g; o[1] = w.l; o[2] = w.tm; o[3] = w.tn; o[4] = w.kt0; o[5] = w.kt1;
@@ -655,7 +698,7 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   if ((rc = noalloc_setup(dev, &nd)) != NVFP4_OK) return rc;
 
   Plan pl;
-  if ((rc = make_plan(1, &M, &N, &K, &L, nd->sms, &pl)) != NVFP4_OK) return rc;
+  if ((rc = make_plan(1, &M, &N, &K, &L, nd->sms, &pl, /*allow_cluster=*/false)) != NVFP4_OK) return rc;
   if (pl.workspace_bytes > kNoAllocPartialBytes || pl.counters > kNoAllocCounters)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "this problem needs %zu bytes of stream-K scratch and %d tile counters; the static "
@@ -687,7 +730,7 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   const size_t clear = kNoAllocHeader + static_cast<size_t>(pl.counters) * sizeof(int);
   if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
-  e = gemm_launch(pl.bn, p, pl.grid, stream, false);  // follows a memset: plain launch
+  e = gemm_launch(pl.bn, 1, p, pl.grid, stream, false);  // follows a memset: plain launch
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }

@@ -293,5 +293,50 @@ __device__ __forceinline__ void tc_mma_nvf4_elect(uint32_t d_tmem, uint64_t a_de
       : "memory");
 }
 
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of every CTA of the cluster (hardware barrier; every CTA of a
+// cluster is co-scheduled, so it completes once each CTA arrives).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 3-D tiled load delivered to the same shared-memory offset of every CTA in
+// `cta_mask`; each destination CTA's mbarrier at `bar` counts the bytes.
+__device__ __forceinline__ void tma_load_3d_mc_elect(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                     int z, uint32_t bar, uint64_t policy,
+                                                     uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6, %7;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_mc_elect(uint32_t dst, const void* src, uint32_t bytes,
+                                                   uint32_t bar, uint64_t policy, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4, %5;\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "h"(cta_mask), "l"(policy)
+      : "memory");
+}
+
+// Commit whose arrival lands on the mbarrier at `bar` in every CTA of `cta_mask`.
+__device__ __forceinline__ void tc_commit_mc_elect(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 }  // namespace ptx
 }  // namespace nvfp4

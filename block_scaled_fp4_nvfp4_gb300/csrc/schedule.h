@@ -33,6 +33,7 @@ struct Schedule {
   int dp_tiles;     // tiles [0, dp_tiles) run whole, tile c + i*grid on CTA c
   long long sk_iters;  // T: total stream-K iterations (0 = no stream-K part)
   int sk_max_segs;  // workspace slots reserved per stream-K tile
+  int cluster;      // CTAs per cluster (1, or 2: the pair runs tiles 2q, 2q+1, sharing B)
 };
 
 struct Work {
@@ -43,7 +44,8 @@ struct Work {
 };
 
 struct WorkCursor {
-  int dp_next;
+  int dp_next;  // next data-parallel tile group (one tile per cluster rank)
+  int rank;     // rank inside the cluster
   long long x, hi;
 };
 
@@ -52,8 +54,12 @@ NVFP4_HD int sk_owner(long long y, long long T, int G) {
   return static_cast<int>(((y + 1) * G - 1) / T);
 }
 
-NVFP4_HD void work_begin(const Schedule& s, int cta, int grid, WorkCursor& cur) {
+// `cta` / `grid` count clusters; `rank` is the CTA's rank inside its cluster.
+// With clusters of 2 the plan is data-parallel only and every group has an
+// even number of m-tiles, so tiles 2q and 2q+1 (m fastest) share g, l, tn.
+NVFP4_HD void work_begin(const Schedule& s, int cta, int grid, WorkCursor& cur, int rank = 0) {
   cur.dp_next = cta;
+  cur.rank = rank;
   if (s.sk_iters > 0) {
     cur.x = s.sk_iters * cta / grid;
     cur.hi = s.sk_iters * (cta + 1) / grid;
@@ -76,8 +82,8 @@ NVFP4_HD void tile_coords(const Schedule& s, int t, Work& w) {
 
 // Next piece of work of CTA `cta` (of `grid`); false when done.
 NVFP4_HD bool work_next(const Schedule& s, int cta, int grid, WorkCursor& cur, Work& w) {
-  if (cur.dp_next < s.dp_tiles) {
-    tile_coords(s, cur.dp_next, w);
+  if (cur.dp_next * s.cluster < s.dp_tiles) {
+    tile_coords(s, cur.dp_next * s.cluster + cur.rank, w);
     w.kt0 = 0;
     w.kt1 = s.ktiles[w.g];
     w.seg = 0;

@@ -152,6 +152,8 @@ NVFP4_API int nvfp4_gemm_debug_inject_skip(int ktile);
  *   out[0] BN            out[1] output tiles     out[2] grid (CTAs)
  *   out[3] smem stages   out[4] dp_tiles         out[5] stream-K tiles
  *   out[6] stream-K k-tile iterations            out[7] most CTAs sharing a tile
+ *   out[8] (when out_len >= 9) CTAs per cluster: 2 when pairs of CTAs with the
+ *          same B columns share each B tile through cluster multicast
  */
 NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L,
                     int num_sms, int* out, int out_len);

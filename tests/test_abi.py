@@ -183,3 +183,27 @@ def test_timeout_setting_validated(lib):
     with pytest.raises(binding.Nvfp4Error):
         binding.nvfp4_gemm_set_wait_timeout_ns(10)
     binding.nvfp4_gemm_set_wait_timeout_ns(2_000_000_000)
+
+
+def test_cluster_pairs_share_b_columns(lib, monkeypatch):
+    """Clusters of two CTAs: rank 0 and rank 1 run tiles with the same group,
+    batch and n-tile, adjacent m-tiles and identical k-ranges, in lockstep."""
+    for case in ([8192], [8192], [8192], [1]), ([1024, 2048], [4096, 7168], [7168, 2048], [1, 1]):
+        p = binding.nvfp4_gemm_plan(*case, 152)
+        assert p["cluster"] == 2 and p["grid"] % 2 == 0
+        _check_schedule(*case, 152)
+        for c in range(0, min(p["grid"], 12), 2):
+            w0 = binding.nvfp4_gemm_debug_schedule(*case, 152, c)
+            w1 = binding.nvfp4_gemm_debug_schedule(*case, 152, c + 1)
+            assert len(w0) == len(w1) > 0
+            for a, b in zip(w0, w1):
+                assert (a["g"], a["l"], a["tn"], a["kt0"], a["kt1"]) == (b["g"], b["l"], b["tn"], b["kt0"], b["kt1"])
+                assert b["tm"] == a["tm"] + 1 and a["tm"] % 2 == 0
+    # odd m-tile counts, stream-K plans and the override fall back to single CTAs
+    assert binding.nvfp4_gemm_plan([384, 64], [4096, 4096], [7168, 7168], [1, 1], 152)["cluster"] == 1
+    assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["cluster"] == 1
+    monkeypatch.setenv("NVFP4_CLUSTER", "1")
+    assert binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)["cluster"] == 1
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    p = binding.nvfp4_gemm_plan([256], [512], [1024], [1], 152)
+    assert p["cluster"] == 1 or p["dp_tiles"] == p["tiles"]

@@ -200,3 +200,48 @@ def test_parity_wide_tiles(mode, M, N, K, L, monkeypatch):
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, L)
+
+
+@pytest.mark.parametrize("bn", ["128", "256"])
+@pytest.mark.parametrize("M,N,K,L", [(256, 512, 1024, 1), (512, 1024, 2048, 1), (200, 264, 512, 2),
+                                     (1024, 136, 768, 1)])
+def test_parity_cluster_pairs(bn, M, N, K, L, monkeypatch):
+    """Clusters of two CTAs sharing each B tile through multicast."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", bn)
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    plan = binding.nvfp4_gemm_plan([M], [N], [K], [L], torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["cluster"] == 2
+    p = workloads.make_random_problem(M + N + 5 * K + int(bn), M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
+
+
+def test_cluster_timeout_is_reported(monkeypatch):
+    """A skipped k-tile in a cluster pair: both CTAs give up, the host sees it."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    M, N, K = 256, 512, 1024
+    p = workloads.make_random_problem(5, M, N, K)
+    d = to_device(p)
+    try:
+        binding.nvfp4_gemm_set_wait_timeout_ns(50_000_000)
+        binding.nvfp4_gemm_debug_inject_skip(1)
+        _, C = alloc_c(M, N, 1)
+        run_single(d, C)
+        with pytest.raises(binding.Nvfp4Error) as e:
+            binding.nvfp4_gemm_check_device_status()
+        assert e.value.code == -4
+    finally:
+        binding.nvfp4_gemm_debug_inject_skip(-1)
+        binding.nvfp4_gemm_set_wait_timeout_ns(2_000_000_000)
+    _, C = alloc_c(M, N, 1)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
