@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     while (left > 0 && work_next(p.sched, unit, units, pc, pw)) {
       const size_t atoms = static_cast<size_t>(p.sched.ktiles[pw.g]) * 4;
       const uint8_t* sfa = p.sfa[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_a[pw.g] + pw.tm) * atoms * kSfAtomBytes;
-      const int sfb_block0 = pw.tn * Cfg::kSfbBlocks;
+      const int sfb_block0 = pw.tn * BN / 128;
       const uint8_t* sfb = p.sfb[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_b[pw.g] + sfb_block0) * atoms * kSfAtomBytes;
       for (int kt = pw.kt0; kt < pw.kt1 && left > 0; ++kt, --left) {
         ptx::prefetch_tile_l2_3d(&p.tmA[pw.g], kt * kBKBytes, pw.tm * kBM, pw.l);
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       const size_t atoms_per_block = static_cast<size_t>(p.sched.ktiles[x.g]) * 4;
       const uint8_t* sfa = p.sfa[x.g] +
           (static_cast<size_t>(x.l) * p.sf_rows_a[x.g] + x.tm) * atoms_per_block * kSfAtomBytes;
-      const int sfb_block0 = x.tn * Cfg::kSfbBlocks;
+      const int sfb_block0 = x.tn * BN / 128;  // 128-row scale block holding the tile's first row
       const uint8_t* sfb = p.sfb[x.g] +
           (static_cast<size_t>(x.l) * p.sf_rows_b[x.g] + sfb_block0) * atoms_per_block * kSfAtomBytes;
       int nsfb = p.sf_rows_b[x.g] - sfb_block0;
@@ -321,6 +321,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         const uint32_t sSFA = sB + Cfg::kBBytes;
         const uint32_t sSFB = sSFA + kSfSlabBytes;
         const uint32_t sfa_t = tmem + Cfg::kSfBaseCol + slot * Cfg::kSfSlotCols;
+        // A 64-wide tile uses the upper half of its 128-row B scale atom when
+        // it starts at row 64 of the atom: column j holds rows 32j..32j+31
+        // ("nvfp4 group gemm, submission 407526": sfb_lane).
+        const uint32_t sfb_col0 = BN < 128 ? static_cast<uint32_t>((x.tn * BN) % 128 / 32) : 0u;
         const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
         // Scale atoms -> tensor memory.  Atom kb of a 128-row block holds the
         // 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
@@ -329,14 +333,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           ptx::tc_copy_sf_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
 #pragma unroll
           for (int j = 0; j < Cfg::kSfbBlocks; ++j)
-            ptx::tc_copy_sf_elect(sfb_t + kb * (BN / 32) + 4 * j,
+            ptx::tc_copy_sf_elect(sfb_t + kb * Cfg::kSfbKbCols + 4 * j,
                                   scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes));
         }
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
           // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
           ptx::tc_mma_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
-                                 sfa_t + 4 * kb, sfb_t + kb * (BN / 32),
+                                 sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0,
                                  (kt > x.kt0 || kb > 0) ? 1u : 0u);
         }
         if constexpr (CL == 1)
@@ -487,14 +491,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       // ...), so the result does not depend on which segment finished last.
       const float4* ws0 = reinterpret_cast<const float4*>(p.workspace) + sk_slot(p.sched, x, 0) * (BN / 4 * kBM) + row;
       constexpr int kMaxSeg = 4;  // loads of up to 4 segments in flight at once
+      // Sum 128 columns at a time into packed fp16 registers before storing
+      // them, so the loads of all four 32-column groups are in flight together.
+      constexpr int kPassCols = BN < 128 ? BN : 128;
 #pragma unroll 1
-      for (int q = 0; q < BN / 64; ++q) {
-        float v[64];
+      for (int c0 = 0; c0 < BN; c0 += kPassCols) {
+        uint32_t hs[kPassCols / 2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // 32-column halves
+        for (int c = 0; c < kPassCols / 32; ++c) {  // 32-column groups
           float4 acc[8];
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) acc[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int cg = c0 / 4 + 8 * c;  // first 4-column group of this 32-column group
           for (int j0 = 0; j0 < x.nseg; j0 += kMaxSeg) {
             float4 part[kMaxSeg][8];
 #pragma unroll
@@ -502,7 +510,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 #pragma unroll
               for (int c4 = 0; c4 < 8; ++c4)
                 part[j][c4] = (j0 + j < x.nseg)
-                    ? __ldcg(ws0 + static_cast<size_t>(j0 + j) * (BN / 4 * kBM) + (16 * q + 8 * h + c4) * kBM)
+                    ? __ldcg(ws0 + static_cast<size_t>(j0 + j) * (BN / 4 * kBM) + (cg + c4) * kBM)
                     : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < kMaxSeg; ++j)
@@ -517,13 +525,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           }
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            v[32 * h + 4 * c4] = acc[c4].x;
-            v[32 * h + 4 * c4 + 1] = acc[c4].y;
-            v[32 * h + 4 * c4 + 2] = acc[c4].z;
-            v[32 * h + 4 * c4 + 3] = acc[c4].w;
+            hs[16 * c + 2 * c4] = pack_half2(acc[c4].x, acc[c4].y);
+            hs[16 * c + 2 * c4 + 1] = pack_half2(acc[c4].z, acc[c4].w);
           }
         }
-        if (rows_live) store_chunk(x, q, v);
+        if (rows_live) {
+#pragma unroll
+          for (int c = 0; c < kPassCols / 32; ++c) store_box(x, c0 + 32 * c, &hs[16 * c]);
+        }
       }
       // The partials are consumed: drop their L2 lines without writing them
       // back.  This warp read exactly the lines of its own 32 rows.
@@ -608,6 +617,7 @@ static int max_clusters_bn() {
 cudaError_t gemm_prepare_device(int bn) {
   cudaError_t e;
   switch (bn) {
+    case 64: return prepare_bn<64, 1>();
     case 128:
       if ((e = prepare_bn<128, 1>()) != cudaSuccess) return e;
       return prepare_bn<128, 2>();
@@ -627,6 +637,7 @@ cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cuda
     }
   }
   switch (bn) {
+    case 64: return launch_bn<64, 1>(p, grid, stream, pdl);
     case 128: return launch_bn<128, 1>(p, grid, stream, pdl);
     case 256: return launch_bn<256, 1>(p, grid, stream, pdl);
     default: return cudaErrorInvalidValue;
@@ -640,6 +651,7 @@ int gemm_max_clusters(int bn, int cluster) {
 
 int gemm_stages(int bn) {
   switch (bn) {
+    case 64: return TileCfg<64>::kStages;
     case 128: return TileCfg<128>::kStages;
     case 256: return TileCfg<256>::kStages;
     default: return 0;

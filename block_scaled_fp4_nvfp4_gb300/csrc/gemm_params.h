@@ -77,8 +77,13 @@ struct TileCfg {
   static constexpr int kDynSmem = kStages * kStageBytes + kEpiBytes + 1024;  // +1024 alignment slack
   // Tensor memory: accumulators first, then a ring of scale slots.
   static constexpr int kAccBufs = (BN <= 128) ? 2 : 1;
+  static_assert(BN == 64 || BN % 128 == 0, "tile widths: 64, 128, 256");
   static constexpr int kSfaCols = 4 * (kBK / kMmaK);               // 16 per k-tile
-  static constexpr int kSfbCols = (BN / 32) * (kBK / kMmaK);       // BN/32 per MMA
+  // B scale columns per MMA k-block: BN/32, but a whole 4-column atom is
+  // copied even when the tile is narrower than the 128-row atom (BN = 64: the
+  // MMA reads the half of the atom that holds its rows).
+  static constexpr int kSfbKbCols = BN / 32 > 4 ? BN / 32 : 4;
+  static constexpr int kSfbCols = kSfbKbCols * (kBK / kMmaK);
   static constexpr int kSfSlots = kStages;  // one tensor-memory scale slot per smem stage
   static constexpr int kSfSlotCols = kSfaCols + kSfbCols;
   static constexpr int kSfBaseCol = kAccBufs * BN;

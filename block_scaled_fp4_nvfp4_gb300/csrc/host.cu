@@ -69,7 +69,7 @@ struct DeviceState {
   int sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;       // device status word
-  bool prepared_bn[2] = {false, false};  // BN = 128, 256
+  bool prepared_bn[3] = {false, false, false};  // BN = 128, 256, 64
   int max_clusters[2] = {0, 0};          // co-resident 2-CTA clusters, BN = 128, 256
 };
 
@@ -248,7 +248,7 @@ constexpr int kMinSkIters = 4;
 int choose_bn(int G, const int* M, const int* N, const int* L, int sms) {
   if (const char* env = getenv("NVFP4_BN")) {
     const int v = atoi(env);
-    if (v == 128 || v == 256) return v;
+    if (v == 64 || v == 128 || v == 256) return v;
   }
   long long tiles256 = 0;
   for (int g = 0; g < G; ++g) tiles256 += cdiv(M[g], kBM) * cdiv(N[g], 256) * L[g];
@@ -259,8 +259,8 @@ int choose_bn(int G, const int* M, const int* N, const int* L, int sms) {
 // halve the B tiles' L2 -> SM traffic.  Used for data-parallel plans whose
 // groups all have an even number of 128-row m-tiles and at least two waves of
 // tiles; NVFP4_CLUSTER = 1 | 2 overrides (2 only where the pairing is valid).
-int choose_cluster(const Schedule& s, int sms, bool allow) {
-  if (!allow || sms < 2 || s.dp_tiles != s.total_tiles) return 1;
+int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
+  if (!allow || sms < 2 || s.dp_tiles != s.total_tiles || bn < 128) return 1;
   for (int g = 0; g < s.num_groups; ++g)
     if (s.tiles_m[g] % 2 != 0) return 1;
   int want = s.total_tiles >= 2 * sms ? 2 : 1;
@@ -357,7 +357,7 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
   }
   if (pl->grid < 1) pl->grid = 1;
   s.cluster = 1;
-  pl->cluster = choose_cluster(s, sms, allow_cluster);
+  pl->cluster = choose_cluster(s, sms, allow_cluster, pl->bn);
   if (pl->cluster > 1) {
     s.cluster = pl->cluster;
     const long long groups = tiles / pl->cluster;
@@ -479,7 +479,7 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
       pl.grid = mc * pl.cluster;
     }
   }
-  const int bn_i = pl.bn == 256 ? 1 : 0;
+  const int bn_i = pl.bn == 256 ? 1 : pl.bn == 64 ? 2 : 0;
   if (!ds->prepared_bn[bn_i]) {
     if ((e = gemm_prepare_device(pl.bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     ds->prepared_bn[bn_i] = true;
@@ -672,6 +672,7 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
       return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
     if ((e = gemm_prepare_device(128)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     if ((e = gemm_prepare_device(256)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    if ((e = gemm_prepare_device(64)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     d.scratch = static_cast<unsigned char*>(ptr);
     d.ready = true;
   }

@@ -245,3 +245,21 @@ def test_cluster_timeout_is_reported(monkeypatch):
     run_single(d, C)
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
+
+
+@pytest.mark.parametrize("mode", ["dp", "sk"])
+@pytest.mark.parametrize("M,N,K,L", [(128, 448, 2048, 1), (200, 136, 512, 2), (64, 264, 1024, 1),
+                                     (256, 192, 768, 1)])
+def test_parity_narrow_tiles(mode, M, N, K, L, monkeypatch):
+    """128 x 64 output tiles: an odd n-tile reads the upper half of its
+    128-row B scale atom."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", "64")
+    monkeypatch.setenv("NVFP4_SCHEDULE", mode)
+    p = workloads.make_random_problem(7 * M + N + K, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
