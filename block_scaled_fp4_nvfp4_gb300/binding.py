@@ -170,10 +170,11 @@ def nvfp4_gemm_plan(M, N, K, L, num_sms):
     """Host-only launch plan (see include/nvfp4_gemm.h) as a dict."""
     G = len(M)
     ia = lambda xs: (ctypes.c_int * G)(*[int(v) for v in xs])
-    out = (ctypes.c_int * 9)()
-    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 9)
+    out = (ctypes.c_int * 10)()
+    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 10)
     _check(rc, "nvfp4_gemm_plan")
-    keys = ("bn", "tiles", "grid", "stages", "dp_tiles", "sk_tiles", "sk_iters", "sk_max_segs", "cluster")
+    keys = ("bn", "tiles", "grid", "stages", "dp_tiles", "sk_tiles", "sk_iters", "sk_max_segs", "cluster",
+            "pair")
     return dict(zip(keys, list(out)))
 
 

@@ -108,13 +108,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 }  // namespace
 
-template <int BN, int CL>
+template <int BN, int CL, bool P2>
 __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = TileCfg<BN>;
+  using Cfg = TileCfg<BN, P2>;
   static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
-  // CL == 2: the two CTAs of a cluster run tiles with the same B columns;
-  // each loads half of every B tile and of the B scale slabs and multicasts
-  // it to both, halving B's L2 -> SM traffic.
+  static_assert(!P2 || CL == 2, "2-SM pairs are clusters of two CTAs");
+  // CL == 2: the two CTAs of a cluster run tiles with the same B columns
+  // (m-tiles 2q and 2q+1).  Without P2 each loads half of every B tile and
+  // of the B scale slabs and multicasts it to both, halving B's L2 -> SM
+  // traffic.  With P2 the pair runs one 256 x BN tile as 2-SM MMAs
+  // (tcgen05 cta_group::2, issued by the even CTA): each CTA keeps only its
+  // half of B in shared memory, the tensor cores exchange the halves, and
+  // every copy of both CTAs is counted on the leader's "full" barrier.
   constexpr uint16_t kPeers = static_cast<uint16_t>((1u << CL) - 1u);
   constexpr int kBHalfRows = BN / CL;
   constexpr int kStages = Cfg::kStages;
@@ -141,11 +146,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), CL);  // released by the MMAs of every CTA that reads it
+      ptx::mbar_init(empty_bar(s), P2 ? 1 : CL);  // released by the MMAs of every CTA that reads it
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full_bar(b), 1);
-      ptx::mbar_init(acc_empty_bar(b), kEpiWarps);
+      ptx::mbar_init(acc_empty_bar(b), kEpiWarps * (P2 ? 2 : 1));  // pairs: both CTAs' epilogues
     }
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_gather), kEpiWarps);
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_bcast), 1);
@@ -159,11 +164,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       ptx::prefetch_tensormap(&p.tmA[g]);
       ptx::prefetch_tensormap(&p.tmB[g]);
       ptx::prefetch_tensormap(&p.tmC[g]);
+      if constexpr (P2) {
+        ptx::prefetch_tensormap(&p.tmSFA[g]);
+        ptx::prefetch_tensormap(&p.tmSFB[g]);
+      }
     }
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), Cfg::kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (P2) {
+      ptx::tmem_alloc2(ptx::smem_addr(&ctl.tmem_base), Cfg::kTmemCols);
+      ptx::tmem_relinquish2();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl.tmem_base), Cfg::kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
@@ -234,6 +248,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           (static_cast<size_t>(x.l) * p.sf_rows_b[x.g] + sfb_block0) * atoms_per_block * kSfAtomBytes;
       int nsfb = p.sf_rows_b[x.g] - sfb_block0;
       nsfb = nsfb < Cfg::kSfbBlocks ? nsfb : Cfg::kSfbBlocks;
+      // pair copies of the scale slabs: rows of 256 B in the 2-D scale maps
+      const int sfa_row = static_cast<int>(atoms_per_block / 4 * 8) * (x.l * p.sf_rows_a[x.g] + x.tm);
+      const int sfb_row = static_cast<int>(atoms_per_block / 4 * 8) * (x.l * p.sf_rows_b[x.g] + sfb_block0);
       const uint32_t stage_tx =
           Cfg::kABytes + Cfg::kBBytes + kSfSlabBytes + static_cast<uint32_t>(nsfb) * kSfSlabBytes;
       for (int kt = x.kt0; kt < x.kt1; ++kt) {
@@ -249,7 +266,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           armed[stage] = -1;  // test-only: nothing issued, nothing in flight
         } else {
           const uint32_t fb = full_bar(stage);
-          if (warp == 0) {
+          if constexpr (P2) {
+            // Every copy of both CTAs lands on the leader's barrier, armed by
+            // the leader with both CTAs' bytes.  Both B scale slabs go to each
+            // CTA (each tensor core scales all BN columns); a slab past the
+            // last 128-row block reads other scales or zeros, harmless since
+            // those B rows are zero-filled and their columns are not stored.
+            const uint32_t lfb = ptx::mapa_shared(fb, 0);
+            if (warp == 0) {
+              if (crank == 0) ptx::mbar_arrive_expect_tx_elect(fb, 2u * Cfg::kStageBytes);
+              ptx::tma_load_3d_pair_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, lfb, polA);
+              ptx::tma_load_2d_pair_elect(sSFA, &p.tmSFA[x.g], 0, sfa_row + kt * 8, lfb, polA);
+            } else {
+              ptx::tma_load_3d_pair_elect(sB, mapB, kt * kBKBytes, x.tn * BN + crank * kBHalfRows, x.l, lfb, polB);
+#pragma unroll
+              for (int j = 0; j < Cfg::kSfbBlocks; ++j)
+                ptx::tma_load_2d_pair_elect(sSFB + j * kSfSlabBytes, &p.tmSFB[x.g], 0,
+                                            sfb_row + static_cast<int>(atoms_per_block / 4 * 8) * j + kt * 8,
+                                            lfb, polB);
+            }
+          } else if (warp == 0) {
             ptx::mbar_arrive_expect_tx_elect(fb, stage_tx);
             ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
             ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
@@ -277,8 +313,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         }
       }
     }
-    if (!ok) {
-      // Shutting down: wait for the copies this warp put in flight.
+    if (!ok && (!P2 || crank == 0)) {
+      // Shutting down: wait for the copies this warp put in flight.  (A pair's
+      // odd CTA cannot wait on the leader's barriers; it lingers before
+      // exiting instead, see the end of the kernel.)
       if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
@@ -286,11 +324,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       }
       __syncwarp();
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp && (!P2 || crank == 0)) {
     // ------------------------------------------------------------ MMA issuer
     // Whole warp in the loop, one elected lane issues every tcgen05 operation
-    // (always the same lane, so its commits track all of them).
-    constexpr uint32_t idesc = make_idesc_nvf4(kBM, BN);
+    // (always the same lane, so its commits track all of them).  In a 2-SM
+    // pair only the even CTA's MMA warp runs; its MMAs, scale copies and
+    // commits act on both CTAs.
+    constexpr uint32_t idesc = make_idesc_nvf4(P2 ? 2 * kBM : kBM, BN);
     int stage = 0;
     uint32_t phase = 0;
     int ab = 0;
@@ -330,20 +370,34 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
-          ptx::tc_copy_sf_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+          if constexpr (P2)
+            ptx::tc_copy_sf2_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+          else
+            ptx::tc_copy_sf_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
 #pragma unroll
-          for (int j = 0; j < Cfg::kSfbBlocks; ++j)
-            ptx::tc_copy_sf_elect(sfb_t + kb * Cfg::kSfbKbCols + 4 * j,
-                                  scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes));
+          for (int j = 0; j < Cfg::kSfbBlocks; ++j) {
+            const uint32_t t = sfb_t + kb * Cfg::kSfbKbCols + 4 * j;
+            const uint64_t d = scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes);
+            if constexpr (P2)
+              ptx::tc_copy_sf2_elect(t, d);
+            else
+              ptx::tc_copy_sf_elect(t, d);
+          }
         }
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
           // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
-          ptx::tc_mma_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
-                                 sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0,
-                                 (kt > x.kt0 || kb > 0) ? 1u : 0u);
+          const uint32_t acc = (kt > x.kt0 || kb > 0) ? 1u : 0u;
+          if constexpr (P2)
+            ptx::tc_mma2_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
+                                    sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols, acc);
+          else
+            ptx::tc_mma_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
+                                   sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
         }
-        if constexpr (CL == 1)
+        if constexpr (P2)
+          ptx::tc_commit2_mc_elect(empty_bar(stage), kPeers);  // the stage is free in both CTAs
+        else if constexpr (CL == 1)
           ptx::tc_commit_elect(empty_bar(stage));
         else
           ptx::tc_commit_mc_elect(empty_bar(stage), kPeers);  // the stage is free once both CTAs read it
@@ -353,7 +407,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         }
       }
       if (!ok) break;
-      ptx::tc_commit_elect(acc_full_bar(ab));
+      if constexpr (P2)
+        ptx::tc_commit2_mc_elect(acc_full_bar(ab), kPeers);  // each CTA's epilogue drains its own rows
+      else
+        ptx::tc_commit_elect(acc_full_bar(ab));
       if (++ab == Cfg::kAccBufs) {
         ab = 0;
         aphase ^= 1u;
@@ -361,11 +418,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     }
     if (!ok) {
       const uint32_t drain_bar = ptx::smem_addr(&ctl.mma_drain);
-      ptx::tc_commit_elect(drain_bar);
+      if constexpr (P2)
+        ptx::tc_commit2_mc_elect(drain_bar, 1);
+      else
+        ptx::tc_commit_elect(drain_bar);
       if (lane == 0) W.drain(drain_bar, 0);
       __syncwarp();
     }
-  } else {
+  } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - kFirstEpiWarp;  // epilogue warp 0..3
     const int sub = warp & 3;          // tensor-memory sub-partition this warp may read
@@ -430,7 +490,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       auto release_acc = [&]() {
         ptx::tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(acc_empty_bar(my_ab));
+        if (lane == 0) {
+          if constexpr (P2)
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(my_ab), 0));  // the leader's MMAs wait
+          else
+            ptx::mbar_arrive(acc_empty_bar(my_ab));
+        }
       };
 
       if (x.nseg == 1) {
@@ -551,17 +616,35 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   ptx::tc_fence_before_sync();
   __syncthreads();
+  if constexpr (P2) {
+    // After an abort a pair CTA may still have copies in flight that only the
+    // leader's barriers count: give them time to land before the shared
+    // memory goes away (they are plain reads of the operands; microseconds).
+    if (ctl.abort) {
+      if (threadIdx.x == 0) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 200000ull) {
+        }
+      }
+      __syncthreads();
+    }
+  }
   // No CTA leaves while its peer may still multicast into its shared memory
   // or signal its barriers.
   if constexpr (CL > 1) ptx::cluster_sync();
   ptx::tc_fence_after_sync();
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+  if (warp == kMmaWarp) {
+    if constexpr (P2)
+      ptx::tmem_dealloc2(tmem, Cfg::kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------- launcher
-template <int BN, int CL>
+template <int BN, int CL, bool P2 = false>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  using Cfg = TileCfg<BN>;
+  using Cfg = TileCfg<BN, P2>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
@@ -586,22 +669,22 @@ static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, CL>, p);
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, CL, P2>, p);
 }
 
-template <int BN, int CL>
+template <int BN, int CL, bool P2 = false>
 static cudaError_t prepare_bn() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TileCfg<BN>::kDynSmem);
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, CL, P2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<BN, P2>::kDynSmem);
 }
 
 // Largest number of co-resident clusters of CL CTAs (0 on error).
-template <int BN, int CL>
+template <int BN, int CL, bool P2 = false>
 static int max_clusters_bn() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL * 1024, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
-  cfg.dynamicSmemBytes = TileCfg<BN>::kDynSmem;
+  cfg.dynamicSmemBytes = TileCfg<BN, P2>::kDynSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
@@ -610,7 +693,7 @@ static int max_clusters_bn() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<BN, CL>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<BN, CL, P2>, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
@@ -623,12 +706,15 @@ cudaError_t gemm_prepare_device(int bn) {
       return prepare_bn<128, 2>();
     case 256:
       if ((e = prepare_bn<256, 1>()) != cudaSuccess) return e;
-      return prepare_bn<256, 2>();
+      if ((e = prepare_bn<256, 2>()) != cudaSuccess) return e;
+      return prepare_bn<256, 2, true>();
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
+cudaError_t gemm_launch(int bn, int cluster, bool pair, const GemmParams& p, int grid, cudaStream_t stream,
+                        bool pdl) {
+  if (pair) return (cluster == 2 && bn == 256) ? launch_bn<256, 2, true>(p, grid, stream, pdl) : cudaErrorInvalidValue;
   if (cluster == 2) {
     switch (bn) {
       case 128: return launch_bn<128, 2>(p, grid, stream, pdl);
@@ -644,12 +730,14 @@ cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cuda
   }
 }
 
-int gemm_max_clusters(int bn, int cluster) {
+int gemm_max_clusters(int bn, int cluster, bool pair) {
   if (cluster != 2) return 0;
+  if (pair) return bn == 256 ? max_clusters_bn<256, 2, true>() : 0;
   return bn == 256 ? max_clusters_bn<256, 2>() : max_clusters_bn<128, 2>();
 }
 
-int gemm_stages(int bn) {
+int gemm_stages(int bn, bool pair) {
+  if (pair) return bn == 256 ? TileCfg<256, true>::kStages : 0;
   switch (bn) {
     case 64: return TileCfg<64>::kStages;
     case 128: return TileCfg<128>::kStages;

@@ -43,6 +43,11 @@ struct GemmParams {
   CUtensorMap tmA[kMaxGroups];   // uint8 {K/2, M, L}, box {128, 128, 1}, 128B swizzle
   CUtensorMap tmB[kMaxGroups];   // uint8 {K/2, N, L}, box {128, BN, 1}, 128B swizzle
   CUtensorMap tmC[kMaxGroups];   // fp16 {N, M, L}, box {32, 32, 1}, 64B swizzle
+  // Repacked scales as uint8 {256, bytes/256}, box {256, 8} = one 2 KB slab.
+  // Encoded only for 2-SM pair launches, whose copies must signal the pair's
+  // leader CTA (only the tensor form of the bulk copy can).
+  CUtensorMap tmSFA[kMaxGroups];
+  CUtensorMap tmSFB[kMaxGroups];
   const uint8_t* sfa[kMaxGroups];  // repacked scales
   const uint8_t* sfb[kMaxGroups];
   int M[kMaxGroups], N[kMaxGroups];
@@ -58,17 +63,19 @@ struct GemmParams {
   int prefetch_ktiles;           // k-tiles per CTA prefetched into L2 before the launch dependency wait
 };
 
-// Per-BN compile-time configuration.
-template <int BN>
+// Per-BN compile-time configuration.  P2: 2-SM pair tiles (tcgen05
+// cta_group::2, M = 256 across the two CTAs of a cluster): each CTA holds its
+// 128 rows of A, half of the BN rows of B and the B scales of all BN rows.
+template <int BN, bool P2 = false>
 struct TileCfg {
   static constexpr int kBN = BN;
   static constexpr int kABytes = kBM * kBKBytes;               // 16 KB
-  static constexpr int kBBytes = BN * kBKBytes;                // BN * 128 B
+  static constexpr int kBBytes = (P2 ? BN / 2 : BN) * kBKBytes; // B rows held by this CTA x 128 B
   static constexpr int kSfbBlocks = (BN + 127) / 128;          // 128-row scale blocks
   static constexpr int kStageBytes = kABytes + kBBytes + kSfSlabBytes + kSfbBlocks * kSfSlabBytes;
   // Epilogue staging: one 32 rows x 32 fp16 box (64-byte swizzle) per
   // epilogue warp, so that shared memory goes to the operand ring instead
-  // (4 stages at BN = 256, 6 at BN = 128).
+  // (4 stages at BN = 256, 6 at BN = 128, 5 for 2-SM pairs at BN = 256).
   static constexpr int kEpiBoxCols = 32;
   static constexpr int kEpiBufBytes = 32 * kEpiBoxCols * 2;     // 2 KB
   static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
@@ -78,6 +85,7 @@ struct TileCfg {
   // Tensor memory: accumulators first, then a ring of scale slots.
   static constexpr int kAccBufs = (BN <= 128) ? 2 : 1;
   static_assert(BN == 64 || BN % 128 == 0, "tile widths: 64, 128, 256");
+  static_assert(!P2 || BN == 256, "2-SM pair tiles are 256 x 256");
   static constexpr int kSfaCols = 4 * (kBK / kMmaK);               // 16 per k-tile
   // B scale columns per MMA k-block: BN/32, but a whole 4-column atom is
   // copied even when the tile is narrower than the 128-row atom (BN = 64: the

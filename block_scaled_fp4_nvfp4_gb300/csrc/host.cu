@@ -29,9 +29,10 @@
 
 namespace nvfp4 {
 cudaError_t gemm_prepare_device(int bn);
-cudaError_t gemm_launch(int bn, int cluster, const GemmParams& p, int grid, cudaStream_t stream, bool pdl);
-int gemm_max_clusters(int bn, int cluster);
-int gemm_stages(int bn);
+cudaError_t gemm_launch(int bn, int cluster, bool pair, const GemmParams& p, int grid, cudaStream_t stream,
+                        bool pdl);
+int gemm_max_clusters(int bn, int cluster, bool pair);
+int gemm_stages(int bn, bool pair);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
 }  // namespace nvfp4
 
@@ -70,7 +71,7 @@ struct DeviceState {
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;       // device status word
   bool prepared_bn[3] = {false, false, false};  // BN = 128, 256, 64
-  int max_clusters[2] = {0, 0};          // co-resident 2-CTA clusters, BN = 128, 256
+  int max_clusters[3] = {0, 0, 0};       // co-resident 2-CTA clusters: BN = 128, 256, 2-SM pairs
 };
 
 struct Workspace {
@@ -122,7 +123,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct MapKey {
-  int kind;  // 0 operand, 1 C
+  int kind;  // 0 operand, 2 C, 3 repacked scales
   uintptr_t ptr;
   int rows, cols, L, box_rows;
   bool operator==(const MapKey& o) const {
@@ -192,10 +193,37 @@ int encode_c_map(CUtensorMap* out, void* ptr, int M, int N, int L) {
   return NVFP4_OK;
 }
 
+// Repacked scales seen as rows of 256 bytes; box: 8 rows = one 2 KB slab
+// (one 128-row block, one 256-wide k-tile).  `bytes` is a multiple of 2048.
+int encode_scale_map(CUtensorMap* out, const void* ptr, size_t bytes) {
+  const int rows = static_cast<int>(bytes / 256);
+  MapKey key{3, reinterpret_cast<uintptr_t>(ptr), rows, 256, 1, 8};
+  auto it = g_maps.find(key);
+  if (it != g_maps.end()) {
+    *out = it->second;
+    return NVFP4_OK;
+  }
+  auto fn = encode_fn();
+  if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 8};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled(scales, %zu bytes) failed: %d", bytes, static_cast<int>(r));
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(key, *out);
+  return NVFP4_OK;
+}
+
 // ------------------------------------------------------------------ planning
 struct Plan {
   int bn = 128;
-  int cluster = 1;  // CTAs per cluster (2: pairs sharing B tiles by multicast)
+  int cluster = 1;  // CTAs per cluster (2: pairs sharing B tiles)
+  bool pair = false;  // cluster == 2 as one 256-row tile of 2-SM MMAs (else B multicast)
   int stages = 0;
   int grid = 0;     // CTAs
   int tiles_m[kMaxGroups] = {}, tiles_n[kMaxGroups] = {};
@@ -271,10 +299,19 @@ int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
   return want;
 }
 
+// 2-SM pair tiles (256 x 256, tcgen05 cta_group::2) for clustered plans at
+// BN = 256: each CTA keeps half of B in shared memory, so a stage shrinks
+// from 54 to 38 KB and the ring deepens from 4 to 5 stages.  NVFP4_PAIR = 0
+// keeps the multicast clusters instead.
+bool choose_pair(int cluster, int bn) {
+  if (cluster != 2 || bn != 256) return false;
+  if (const char* env = getenv("NVFP4_PAIR")) return atoi(env) != 0;
+  return true;
+}
+
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl,
               bool allow_cluster = true) {
   pl->bn = choose_bn(G, M, N, L, sms);
-  pl->stages = gemm_stages(pl->bn);
   Schedule& s = pl->sched;
   memset(&s, 0, sizeof s);
   s.num_groups = G;
@@ -364,6 +401,8 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     const long long per_wave = sms / pl->cluster;
     pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * pl->cluster);
   }
+  pl->pair = choose_pair(pl->cluster, pl->bn);
+  pl->stages = gemm_stages(pl->bn, pl->pair);
   return NVFP4_OK;
 }
 
@@ -468,11 +507,12 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
   if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
   if (pl.cluster > 1) {
     // persistent grid: no more clusters than can be co-resident
-    const int bi = pl.bn == 256 ? 1 : 0;
-    if (ds->max_clusters[bi] == 0) ds->max_clusters[bi] = gemm_max_clusters(pl.bn, pl.cluster);
+    const int bi = pl.pair ? 2 : pl.bn == 256 ? 1 : 0;
+    if (ds->max_clusters[bi] == 0) ds->max_clusters[bi] = gemm_max_clusters(pl.bn, pl.cluster, pl.pair);
     const int mc = ds->max_clusters[bi];
     if (mc < 1) {
       pl.cluster = 1;
+      pl.pair = false;
       pl.sched.cluster = 1;
       pl.grid = pl.sched.total_tiles < ds->sms ? pl.sched.total_tiles : ds->sms;
     } else if (pl.grid / pl.cluster > mc) {
@@ -497,6 +537,11 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.N[g] = N[g];
     p.sf_rows_a[g] = static_cast<int>(cdiv(M[g], 128));
     p.sf_rows_b[g] = static_cast<int>(cdiv(N[g], 128));
+    if (pl.pair) {
+      const size_t slabs = static_cast<size_t>(L[g]) * (K[g] / kBK);
+      if ((rc = encode_scale_map(&p.tmSFA[g], SFA[g], slabs * p.sf_rows_a[g] * kSfSlabBytes)) != NVFP4_OK) return rc;
+      if ((rc = encode_scale_map(&p.tmSFB[g], SFB[g], slabs * p.sf_rows_b[g] * kSfSlabBytes)) != NVFP4_OK) return rc;
+    }
     // The larger operand streams through L2 once (evict-first); the smaller,
     // re-read by every tile along the other dimension, is kept (evict-last).
     // Same rule as "nvfp4 group gemm, submission 407526" (cache_A / cache_B).
@@ -515,7 +560,7 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.counters = w->counters;
   }
 
-  e = gemm_launch(pl.bn, pl.cluster, p, pl.grid, stream, true);
+  e = gemm_launch(pl.bn, pl.cluster, pl.pair, p, pl.grid, stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }
@@ -586,6 +631,7 @@ int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* 
   out[6] = pl.sched.sk_iters > 0x7FFFFFFF ? 0x7FFFFFFF : static_cast<int>(pl.sched.sk_iters);
   out[7] = pl.sched.sk_max_segs;
   if (out_len >= 9) out[8] = pl.cluster;
+  if (out_len >= 10) out[9] = pl.pair ? 1 : 0;
   return ok();
 }
 
@@ -731,7 +777,7 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   const size_t clear = kNoAllocHeader + static_cast<size_t>(pl.counters) * sizeof(int);
   if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
-  e = gemm_launch(pl.bn, 1, p, pl.grid, stream, false);  // follows a memset: plain launch
+  e = gemm_launch(pl.bn, 1, false, p, pl.grid, stream, false);  // follows a memset: plain launch
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   return ok();
 }

@@ -153,7 +153,10 @@ NVFP4_API int nvfp4_gemm_debug_inject_skip(int ktile);
  *   out[3] smem stages   out[4] dp_tiles         out[5] stream-K tiles
  *   out[6] stream-K k-tile iterations            out[7] most CTAs sharing a tile
  *   out[8] (when out_len >= 9) CTAs per cluster: 2 when pairs of CTAs with the
- *          same B columns share each B tile through cluster multicast
+ *          same B columns (m-tiles 2q, 2q+1) share each B tile
+ *   out[9] (when out_len >= 10) 1 when such a pair runs as one 256 x BN tile of
+ *          2-SM MMAs (tcgen05 cta_group::2, each CTA holding half of B), 0 when
+ *          the pair shares B through cluster multicast
  */
 NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L,
                     int num_sms, int* out, int out_len);
@@ -173,12 +176,12 @@ NVFP4_API int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const
  * counterpart: this entry point exists for callers that cannot call
  * cudaMalloc -- code running inside a host callback or a custom allocator, a
  * runtime that owns the whole device heap, or a process held to a fixed
- * memory budget -- and so cannot let the library create its split-K
+ * memory budget -- and so cannot let the library create its stream-K
  * workspace on first use.
  *
  * Same arguments, layouts, shape contract and result as nvfp4_gemm_run (one
  * problem).  Stream-K scratch (fp32 partial tiles, per-tile arrival counters,
- * a status word) lives in one static device array of 10 MiB + 16.25 KiB that
+ * a status word) lives in one static device array of 16 MiB + 16.25 KiB that
  * every device which loads this library holds until the process exits.  The
  * first call on a device (with that device current) looks up the array's
  * device address once; make that first call before capturing any stream.

@@ -207,3 +207,20 @@ def test_cluster_pairs_share_b_columns(lib, monkeypatch):
     monkeypatch.setenv("NVFP4_CLUSTER", "2")
     p = binding.nvfp4_gemm_plan([256], [512], [1024], [1], 152)
     assert p["cluster"] == 1 or p["dp_tiles"] == p["tiles"]
+
+
+def test_pair_tiles_planned_for_wide_clusters(lib, monkeypatch):
+    """Clustered 256-wide plans run as 2-SM pair tiles (half of B per CTA, so
+    one more stage fits); NVFP4_PAIR=0 keeps B multicast; 128-wide clusters
+    and single CTAs never pair."""
+    p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
+    assert p["cluster"] == 2 and p["pair"] == 1 and p["stages"] == 5
+    monkeypatch.setenv("NVFP4_PAIR", "0")
+    p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
+    assert p["cluster"] == 2 and p["pair"] == 0 and p["stages"] == 4
+    monkeypatch.delenv("NVFP4_PAIR")
+    monkeypatch.setenv("NVFP4_BN", "128")
+    p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
+    assert p["cluster"] == 2 and p["pair"] == 0
+    monkeypatch.delenv("NVFP4_BN")
+    assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["pair"] == 0

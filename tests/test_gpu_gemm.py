@@ -50,10 +50,21 @@ def test_parity_small(M, N, K, L):
     check_canary(buf, M, N, L)
 
 
-def test_one_hot_scales_pin_the_atom_layout():
+ONE_HOT_CONFIGS = {
+    "auto": {},
+    "wide": {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "1"},
+    "pair": {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2", "NVFP4_PAIR": "1"},
+}
+
+
+@pytest.mark.parametrize("config", sorted(ONE_HOT_CONFIGS))
+def test_one_hot_scales_pin_the_atom_layout(config, monkeypatch):
     """Unit scales except one (row, k-block) per operand: a misplaced scale
-    byte changes exactly the rows/columns it lands in."""
+    byte changes exactly the rows/columns it lands in.  Run for 128-wide
+    tiles, 256-wide tiles and 2-SM pair tiles (whose scales both CTAs copy)."""
     binding = require_gpu()
+    for k, v in ONE_HOT_CONFIGS[config].items():
+        monkeypatch.setenv(k, v)
     M, N, K = 256, 256, 512
     rng = np.random.default_rng(3)
     for trial in range(4):
@@ -222,11 +233,61 @@ def test_parity_cluster_pairs(bn, M, N, K, L, monkeypatch):
     check_canary(buf, M, N, L)
 
 
-def test_cluster_timeout_is_reported(monkeypatch):
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("M,N,K,L", [(256, 512, 1024, 1), (512, 1024, 2048, 1), (200, 264, 512, 2),
+                                     (1024, 136, 768, 1), (256, 256, 256, 1), (768, 520, 1536, 1)])
+def test_parity_pair_tiles(pair, M, N, K, L, monkeypatch):
+    """256 x 256 tiles of two CTAs: 2-SM MMAs with half of B in each CTA
+    (pair=1) or B shared by multicast (pair=0).  Ragged M leaves the odd
+    CTA's rows partly or wholly past M; ragged N leaves the last tile's
+    second scale block past the last row of B."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", "256")
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    monkeypatch.setenv("NVFP4_PAIR", pair)
+    plan = binding.nvfp4_gemm_plan([M], [N], [K], [L], torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["cluster"] == 2 and plan["pair"] == int(pair)
+    p = workloads.make_random_problem(3 * M + N + K + L, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
+
+
+def test_parity_pair_tiles_grouped(monkeypatch):
+    """Grouped problem on 2-SM pair tiles, every group with an even number of
+    m-tiles, against the oracle group by group."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", "256")
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    monkeypatch.delenv("NVFP4_PAIR", raising=False)
+    Ms, Ns, Ks = [256, 512, 200], [512, 264, 1024], [1024, 512, 768]
+    plan = binding.nvfp4_gemm_plan(Ms, Ns, Ks, [1] * 3, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["pair"] == 1
+    probs = [workloads.make_random_problem(900 + g, Ms[g], Ns[g], Ks[g], 1) for g in range(3)]
+    ds = [to_device(p) for p in probs]
+    Cs = [alloc_c(Ms[g], Ns[g], 1) for g in range(3)]
+    binding.nvfp4_gemm_run_grouped(3, [d["A"] for d in ds], [d["B"] for d in ds], [d["SFA"] for d in ds],
+                                   [d["SFB"] for d in ds], [c[1] for c in Cs], Ms, Ns, Ks, [1] * 3)
+    binding.nvfp4_gemm_check_device_status()
+    for g in range(3):
+        assert_close_full(Cs[g][1], probs[g])
+        check_canary(Cs[g][0], Ms[g], Ns[g], 1)
+
+
+@pytest.mark.parametrize("config", ["multicast", "pair"])
+def test_cluster_timeout_is_reported(config, monkeypatch):
     """A skipped k-tile in a cluster pair: both CTAs give up, the host sees it."""
     binding = require_gpu()
     monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
     monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    if config == "pair":
+        monkeypatch.setenv("NVFP4_BN", "256")
+        monkeypatch.setenv("NVFP4_PAIR", "1")
     M, N, K = 256, 512, 1024
     p = workloads.make_random_problem(5, M, N, K)
     d = to_device(p)
