@@ -354,8 +354,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // Scale slot = smem stage: the stage was refilled only after the MMAs
         // that last read this slot completed (they released the stage), so a
         // completed "full" phase also means the slot is free to overwrite.
+        // No tcgen05 fence here: the copies and MMAs only read shared memory
+        // that the completed phase made visible, and a fence per k-tile
+        // would hold back the tensor pipe.
         const int slot = stage;
-        ptx::tc_fence_after_sync();
         const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
         const uint32_t sB = sA + Cfg::kABytes;
         const uint32_t sSFA = sB + Cfg::kBBytes;
@@ -366,8 +368,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // ("nvfp4 group gemm, submission 407526": sfb_lane).
         const uint32_t sfb_col0 = BN < 128 ? static_cast<uint32_t>((x.tn * BN) % 128 / 32) : 0u;
         const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-        // Scale atoms -> tensor memory.  Atom kb of a 128-row block holds the
-        // 4 scales of MMA k-block kb; column j of it holds rows 32j..32j+31.
+        // Per MMA k-block: its scale atoms -> tensor memory, then the MMA, so
+        // the copies of k-block kb+1 can proceed while the MMA of kb runs.
+        // Atom kb of a 128-row block holds the 4 scales of MMA k-block kb;
+        // column j of it holds rows 32j..32j+31.
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
           if constexpr (P2)
@@ -383,9 +387,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
             else
               ptx::tc_copy_sf_elect(t, d);
           }
-        }
-#pragma unroll
-        for (int kb = 0; kb < kBK / kMmaK; ++kb) {
           // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
           const uint32_t acc = (kt > x.kt0 || kb > 0) ? 1u : 0u;
           if constexpr (P2)
