@@ -322,7 +322,9 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     s.tiles_m[g] = pl->tiles_m[g];
     s.tiles_n[g] = pl->tiles_n[g];
     s.L[g] = L[g];
-    s.ktiles[g] = K[g] / kBK;
+    // the last k-tile may be partial (K % 256 = 64, 128 or 192): its loads
+    // read zeros past the end of each row and its scales are zero padding
+    s.ktiles[g] = static_cast<int>(cdiv(K[g], kBK));
     s.tile_start[g] = static_cast<int>(tiles);
     tiles += static_cast<long long>(pl->tiles_m[g]) * pl->tiles_n[g] * L[g];
     if (tiles > 0x3FFFFFFFLL) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "problem has too many output tiles");
@@ -415,8 +417,8 @@ int check_shapes(int G, const int* M, const int* N, const int* K, const int* L) 
     if (M[g] < 1 || N[g] < 1 || K[g] < 1 || L[g] < 1)
       return fail(NVFP4_ERR_INVALID_ARG, "group %d: sizes must be >= 1 (M=%d N=%d K=%d L=%d)", g, M[g],
                   N[g], K[g], L[g]);
-    if (K[g] % kBK != 0)
-      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: K=%d is not a multiple of %d", g, K[g], kBK);
+    if (K[g] % kMmaK != 0)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: K=%d is not a multiple of %d", g, K[g], kMmaK);
     if (N[g] % 8 != 0)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "group %d: N=%d is not a multiple of 8", g, N[g]);
     // tensor-map limits: every dimension < 2^32, byte strides < 2^40
@@ -538,7 +540,7 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.sf_rows_a[g] = static_cast<int>(cdiv(M[g], 128));
     p.sf_rows_b[g] = static_cast<int>(cdiv(N[g], 128));
     if (pl.pair) {
-      const size_t slabs = static_cast<size_t>(L[g]) * (K[g] / kBK);
+      const size_t slabs = static_cast<size_t>(L[g]) * cdiv(K[g], kBK);
       if ((rc = encode_scale_map(&p.tmSFA[g], SFA[g], slabs * p.sf_rows_a[g] * kSfSlabBytes)) != NVFP4_OK) return rc;
       if ((rc = encode_scale_map(&p.tmSFB[g], SFB[g], slabs * p.sf_rows_b[g] * kSfSlabBytes)) != NVFP4_OK) return rc;
     }

@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     NVFP4_OK = 0,
     NVFP4_ERR_INVALID_ARG = -1,       /* null / misaligned pointer, size < 1, G outside 1..8 */
-    NVFP4_ERR_UNSUPPORTED_SHAPE = -2, /* K % 256 != 0, N % 8 != 0, size beyond limits */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = -2, /* K % 64 != 0, N % 8 != 0, size beyond limits */
     NVFP4_ERR_CUDA = -3,              /* a CUDA runtime / driver call failed */
     NVFP4_ERR_DEVICE_TIMEOUT = -4,    /* a kernel's bounded wait ran out (see below) */
     NVFP4_ERR_UNSUPPORTED_DEVICE = -5 /* the current device is not sm_103 */
@@ -93,7 +93,9 @@ NVFP4_API int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int 
  *   A    device [L][M][K/2]       SFA  device, repacked (rows = M)
  *   B    device [L][N][K/2]       SFB  device, repacked (rows = N)
  *   C    device [L][M][N] fp16, written (rows >= M and columns >= N untouched)
- * Shape contract: M, N, K, L >= 1; K % 256 == 0; N % 8 == 0 (16-byte C rows).
+ * Shape contract: M, N, K, L >= 1; K % 64 == 0 (one MMA k-block; a partial
+ * 256-wide k-tile reads zero codes past the end of each row and the zero
+ * padding of the repacked scales); N % 8 == 0 (16-byte C rows).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, UNSUPPORTED_DEVICE, CUDA.
  */
 NVFP4_API int nvfp4_gemm_run(const void* A, const void* B, const void* SFA, const void* SFB, void* C,

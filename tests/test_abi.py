@@ -144,6 +144,31 @@ def test_schedule_forced_modes(lib, mode, monkeypatch):
         assert (p["sk_tiles"] == 0) if mode == "dp" else (p["dp_tiles"] == 0)
 
 
+def test_partial_k_tiles_planned(lib):
+    """K % 256 != 0: the last k-tile of each tile is partial, and the
+    decomposition still covers every k-tile exactly once."""
+    p = binding.nvfp4_gemm_plan([256], [512], [320], [1], 152)
+    assert p["tiles"] == 2 * 4 and p["dp_tiles"] == 0 and p["sk_tiles"] == 8
+    _check_schedule_k([256], [512], [320], [1], 152)
+    _check_schedule_k([128], [7168], [16384 + 64], [1], 152)
+    _check_schedule_k([300, 64], [264, 512], [1088, 192], [2, 1], 152)
+
+
+def _check_schedule_k(M, N, K, L, sms):
+    plan = binding.nvfp4_gemm_plan(M, N, K, L, sms)
+    seen = set()
+    for cta in range(plan["grid"]):
+        for w in binding.nvfp4_gemm_debug_schedule(M, N, K, L, sms, cta):
+            kt = -(-K[w["g"]] // 256)
+            assert 0 <= w["kt0"] < w["kt1"] <= kt
+            for k in range(w["kt0"], w["kt1"]):
+                key = (w["g"], w["l"], w["tm"], w["tn"], k)
+                assert key not in seen
+                seen.add(key)
+    total = sum(-(-M[g] // 128) * -(-N[g] // plan["bn"]) * L[g] * -(-K[g] // 256) for g in range(len(M)))
+    assert len(seen) == total
+
+
 def test_schedule_other_machine_sizes(lib):
     for sms in (1, 7, 148, 160):
         _check_schedule([128], [7168], [16384], [1], sms)
@@ -151,7 +176,8 @@ def test_schedule_other_machine_sizes(lib):
 
 
 @pytest.mark.parametrize("M,N,K,L,code", [
-    (128, 128, 200, 1, -2),   # K % 256
+    (128, 128, 200, 1, -2),   # K % 64
+    (128, 128, 96, 1, -2),    # K % 64
     (128, 100, 256, 1, -2),   # N % 8
     (0, 128, 256, 1, -1),
     (128, 128, 256, 0, -1),

@@ -324,3 +324,50 @@ def test_parity_narrow_tiles(mode, M, N, K, L, monkeypatch):
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, L)
+
+
+PARTIAL_K_CONFIGS = {
+    "auto": {},
+    "dp": {"NVFP4_SCHEDULE": "dp"},
+    "sk": {"NVFP4_SCHEDULE": "sk"},
+    "wide": {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "1"},
+    "narrow": {"NVFP4_BN": "64"},
+}
+
+
+@pytest.mark.parametrize("config", sorted(PARTIAL_K_CONFIGS))
+@pytest.mark.parametrize("M,N,K,L", [(128, 128, 64, 1), (256, 512, 320, 1), (200, 136, 192, 2),
+                                     (512, 1024, 1088, 1), (64, 2048, 4160, 1), (1, 8, 128, 1)])
+def test_parity_partial_k_tiles(config, M, N, K, L, monkeypatch):
+    """K % 256 != 0: the last k-tile is partial (zero codes past the row end,
+    zero-padded scales), under every schedule and tile width."""
+    binding = require_gpu()
+    for k, v in PARTIAL_K_CONFIGS[config].items():
+        monkeypatch.setenv(k, v)
+    p = workloads.make_random_problem(5 * M + N + 3 * K + L, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
+
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 320), (512, 264, 704)])
+def test_parity_partial_k_tiles_pairs(pair, M, N, K, monkeypatch):
+    """Partial last k-tile on 2-CTA tiles (2-SM MMAs or B multicast)."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_BN", "256")
+    monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
+    monkeypatch.setenv("NVFP4_CLUSTER", "2")
+    monkeypatch.setenv("NVFP4_PAIR", pair)
+    plan = binding.nvfp4_gemm_plan([M], [N], [K], [1], torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["cluster"] == 2 and plan["pair"] == int(pair)
+    p = workloads.make_random_problem(M + 7 * N + K, M, N, K, 1)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, 1)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, 1)
