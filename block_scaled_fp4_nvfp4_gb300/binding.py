@@ -69,6 +69,8 @@ def load_library(path=LIB_PATH):
     lib.nvfp4_gemm_plan.restype = i
     lib.nvfp4_gemm_debug_schedule.argtypes = [i, ip, ip, ip, ip, i, i, ip, i]
     lib.nvfp4_gemm_debug_schedule.restype = i
+    lib.nvfp4_gemm_last_launch.argtypes = [ip, i]
+    lib.nvfp4_gemm_last_launch.restype = i
     lib.nvfp4_gemm_encode_idesc.argtypes = [i, i]
     lib.nvfp4_gemm_encode_idesc.restype = ctypes.c_uint32
     lib.nvfp4_gemm_encode_smem_desc.argtypes = [ctypes.c_uint32, i]
@@ -170,12 +172,23 @@ def nvfp4_gemm_plan(M, N, K, L, num_sms):
     """Host-only launch plan (see include/nvfp4_gemm.h) as a dict."""
     G = len(M)
     ia = lambda xs: (ctypes.c_int * G)(*[int(v) for v in xs])
-    out = (ctypes.c_int * 10)()
-    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 10)
+    out = (ctypes.c_int * 11)()
+    rc = load_library().nvfp4_gemm_plan(G, ia(M), ia(N), ia(K), ia(L), num_sms, out, 11)
     _check(rc, "nvfp4_gemm_plan")
     keys = ("bn", "tiles", "grid", "stages", "dp_tiles", "sk_tiles", "sk_iters", "sk_max_segs", "cluster",
-            "pair")
+            "pair", "cluster_reduce")
     return dict(zip(keys, list(out)))
+
+
+LAUNCH_VARIANTS = {-1: None, 0: "single", 1: "multicast", 2: "pair", 3: "cluster_reduce"}
+
+
+def nvfp4_gemm_last_launch():
+    """What this thread's last GEMM launch ran (see include/nvfp4_gemm.h)."""
+    out = (ctypes.c_int * 5)()
+    _check(load_library().nvfp4_gemm_last_launch(out, 5), "nvfp4_gemm_last_launch")
+    return {"bn": out[0], "grid": out[1], "cluster": out[2], "variant": LAUNCH_VARIANTS.get(out[3], out[3]),
+            "stages": out[4]}
 
 
 def nvfp4_gemm_debug_schedule(M, N, K, L, num_sms, cta):

@@ -47,6 +47,8 @@ struct SmemCtl {
   uint64_t epi_gather;
   uint64_t epi_bcast;
   uint64_t mma_drain;
+  uint64_t red_go;    // cluster reduction: every CTA of the cluster may now be written
+  uint64_t red_full;  // cluster reduction: every CTA's slices of this CTA's columns landed
   uint32_t tmem_base;
   volatile int abort;
   int last_flag;
@@ -59,11 +61,17 @@ struct Waiter {
   int* status;
   unsigned long long timeout_ns;
 
+  // kCluster: acquire at cluster scope (the phase was completed by arrivals
+  // that release writes made by other CTAs of the cluster).
+  template <bool kCluster = false>
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int code) const {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto test = [&]() {
+      return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t i = 1;; ++i) {
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (test()) return true;
       if ((i & 7u) == 0) {
         if (*abort_flag) return false;
         if (ptx::globaltimer() - t0 > timeout_ns) {
@@ -89,14 +97,24 @@ struct Waiter {
 // Every lane polls the barrier; the vote makes the outcome warp-uniform and
 // reconverges the warp (a lane that saw the phase complete just as another one
 // gave up still aborts with it).
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(const Waiter& W, uint32_t bar, uint32_t parity, int code) {
-  const bool ok = W.wait(bar, parity, code);
+  const bool ok = W.template wait<kCluster>(bar, parity, code);
   return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -108,11 +126,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 }  // namespace
 
-template <int BN, int CL, bool P2>
+template <int BN, int CL, int MODE>
 __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool P2 = MODE == kModePair;
+  constexpr bool kMc = MODE == kModeMulticast;
+  constexpr bool kRed = MODE == kModeReduce;
   using Cfg = TileCfg<BN, P2>;
-  static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
-  static_assert(!P2 || CL == 2, "2-SM pairs are clusters of two CTAs");
+  static_assert(MODE == kModeSingle ? CL == 1 : (kRed ? (CL == 2 || CL == 4) : CL == 2), "cluster size");
   // CL == 2: the two CTAs of a cluster run tiles with the same B columns
   // (m-tiles 2q and 2q+1).  Without P2 each loads half of every B tile and
   // of the B scale slabs and multicasts it to both, halving B's L2 -> SM
@@ -121,7 +141,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   // half of B in shared memory, the tensor cores exchange the halves, and
   // every copy of both CTAs is counted on the leader's "full" barrier.
   constexpr uint16_t kPeers = static_cast<uint16_t>((1u << CL) - 1u);
-  constexpr int kBHalfRows = BN / CL;
+  constexpr int kBHalfRows = (kMc || P2) ? BN / 2 : BN;  // B rows each CTA of a sharing pair loads
   constexpr int kStages = Cfg::kStages;
   static_assert(kStages <= kMaxStages, "stage ring too deep");
 
@@ -135,8 +155,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int crank = CL > 1 ? static_cast<int>(ptx::cluster_ctarank()) : 0;
-  const int unit = static_cast<int>(blockIdx.x) / CL;   // cluster index
-  const int units = static_cast<int>(gridDim.x) / CL;   // clusters in the grid
+  // Work is dealt per cluster when the cluster shares tiles (multicast, pair)
+  // and per CTA when its CTAs are the segments of one tile (reduce).
+  const int unit = kRed ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) / CL;
+  const int units = kRed ? static_cast<int>(gridDim.x) : static_cast<int>(gridDim.x) / CL;
+  const int wrank = kRed ? 0 : crank;  // rank passed to the work cursor
+  const int brow = (kMc || P2) ? crank * kBHalfRows : 0;  // first B row of the tile this CTA loads
 
   auto full_bar = [&](int s) { return ptx::smem_addr(&ctl.full[s]); };
   auto empty_bar = [&](int s) { return ptx::smem_addr(&ctl.empty[s]); };
@@ -146,7 +170,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), P2 ? 1 : CL);  // released by the MMAs of every CTA that reads it
+      ptx::mbar_init(empty_bar(s), kMc ? CL : 1);  // released by the MMAs of every CTA that reads it
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(acc_full_bar(b), 1);
@@ -155,6 +179,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_gather), kEpiWarps);
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_bcast), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl.mma_drain), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl.red_go), CL);                 // one arrival per CTA of the cluster
+    ptx::mbar_init(ptx::smem_addr(&ctl.red_full), CL * kEpiWarps * 32);  // every epilogue thread of every CTA
     ctl.abort = 0;
     ctl.last_flag = 0;
     ptx::fence_mbar_init();
@@ -192,7 +218,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   // comes after the wait.
   if (warp == 0 && lane == 0 && p.prefetch_ktiles > 0) {
     WorkCursor pc;
-    work_begin(p.sched, unit, units, pc, crank);
+    work_begin(p.sched, unit, units, pc, wrank);
     Work pw;
     int left = p.prefetch_ktiles;
     while (left > 0 && work_next(p.sched, unit, units, pc, pw)) {
@@ -202,7 +228,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       const uint8_t* sfb = p.sfb[pw.g] + (static_cast<size_t>(pw.l) * p.sf_rows_b[pw.g] + sfb_block0) * atoms * kSfAtomBytes;
       for (int kt = pw.kt0; kt < pw.kt1 && left > 0; ++kt, --left) {
         ptx::prefetch_tile_l2_3d(&p.tmA[pw.g], kt * kBKBytes, pw.tm * kBM, pw.l);
-        ptx::prefetch_tile_l2_3d(&p.tmB[pw.g], kt * kBKBytes, pw.tn * BN + crank * kBHalfRows, pw.l);
+        ptx::prefetch_tile_l2_3d(&p.tmB[pw.g], kt * kBKBytes, pw.tn * BN + brow, pw.l);
         ptx::prefetch_l2(sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
         if (sfb_block0 < p.sf_rows_b[pw.g]) ptx::prefetch_l2(sfb + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes);
       }
@@ -233,7 +259,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int count = 0;
     bool ok = true;
     WorkCursor cur;
-    work_begin(p.sched, unit, units, cur, crank);
+    work_begin(p.sched, unit, units, cur, wrank);
     Work x;
     while (ok && work_next(p.sched, unit, units, cur, x)) {
       const CUtensorMap* mapA = &p.tmA[x.g];
@@ -289,7 +315,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
             ptx::mbar_arrive_expect_tx_elect(fb, stage_tx);
             ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
             ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
-          } else if constexpr (CL == 1) {
+          } else if constexpr (!kMc) {
             ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
             for (int j = 0; j < nsfb; ++j)
               ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
@@ -337,7 +363,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     uint32_t aphase = 0;
     bool ok = true;
     WorkCursor cur;
-    work_begin(p.sched, unit, units, cur, crank);
+    work_begin(p.sched, unit, units, cur, wrank);
     Work x;
     while (ok && work_next(p.sched, unit, units, cur, x)) {
       if (!warp_wait(W, acc_empty_bar(ab), aphase ^ 1u, kStatusTimeoutMma)) {
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         }
         if constexpr (P2)
           ptx::tc_commit2_mc_elect(empty_bar(stage), kPeers);  // the stage is free in both CTAs
-        else if constexpr (CL == 1)
+        else if constexpr (!kMc)
           ptx::tc_commit_elect(empty_bar(stage));
         else
           ptx::tc_commit_mc_elect(empty_bar(stage), kPeers);  // the stage is free once both CTAs read it
@@ -436,6 +462,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int ab = 0;
     uint32_t aphase = 0;
     uint32_t gphase = 0;
+    [[maybe_unused]] int red_items = 0;
     // Convert 64 fp32 columns of this thread's row to fp16, stage them as one
     // 128-byte swizzled row of a 32 x 64 box and let lane 0 store the box.
     // Store 32 columns of this warp's 32 rows, packed as 16 half2 words per
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     };
 
     WorkCursor cur;
-    work_begin(p.sched, unit, units, cur, crank);
+    work_begin(p.sched, unit, units, cur, wrank);
     Work x;
     while (work_next(p.sched, unit, units, cur, x)) {
       if (!warp_wait(W, acc_full_bar(ab), aphase, kStatusTimeoutEpilogue)) break;
@@ -514,6 +541,78 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         if (rows_live) {
 #pragma unroll
           for (int c = 0; c < BN / 32; ++c) store_box(x, 32 * c, &h[16 * c]);
+        }
+        continue;
+      }
+
+      if constexpr (kRed) {
+        // The CL segments of this tile are the CL CTAs of this cluster (rank
+        // = segment) and each CTA reduces and stores BN/CL of its columns.
+        // Every CTA writes its fp32 partial of those columns into the owner's
+        // shared memory -- the operand ring, idle once a CTA's only work item
+        // is done -- as [BN/CL/4][128 rows][4], and the owner sums the CL
+        // slices in segment (= k) order, as the workspace path does.
+        constexpr int kOwnCols = BN / CL;
+        constexpr uint32_t kSlotBytes = kOwnCols * kBM * 4;
+        static_assert(kOwnCols % 32 == 0, "whole 32-column boxes per CTA");
+        static_assert(CL * kSlotBytes <= kStages * Cfg::kStageBytes, "reduction slices exceed the ring");
+        if (x.nseg != CL || x.seg != crank || red_items++ != 0) {
+          if (lane == 0) {
+            ctl.abort = 1;
+            atomicCAS(p.status, 0, kStatusBadClusterPlan);
+          }
+          release_acc();
+          break;
+        }
+        const uint32_t go_bar = ptx::smem_addr(&ctl.red_go);
+        const uint32_t rfull_bar = ptx::smem_addr(&ctl.red_full);
+        // This CTA's MMAs are complete (acc_full), so its ring may be written:
+        // tell every CTA of the cluster, then wait until all of them said so.
+        if (ew == 0 && lane < CL) ptx::mbar_arrive_cluster(ptx::mapa_shared(go_bar, static_cast<uint32_t>(lane)));
+        if (!warp_wait<true>(W, go_bar, 0, kStatusTimeoutEpilogue)) break;
+        uint32_t dst[CL];
+#pragma unroll
+        for (int r = 0; r < CL; ++r)
+          dst[r] = ptx::mapa_shared(smem_base + crank * kSlotBytes + row * 16, static_cast<uint32_t>(r));
+#pragma unroll
+        for (int q = 0; q < BN / 64; ++q) {
+          float v[64];
+          load_chunk(t_row + 64 * q, v);
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const int col = 64 * q + 4 * c4;
+            ptx::st_cluster_v4(dst[col / kOwnCols] + (col % kOwnCols) / 4 * (kBM * 16), v[4 * c4], v[4 * c4 + 1],
+                               v[4 * c4 + 2], v[4 * c4 + 3]);
+          }
+        }
+        release_acc();
+        // This thread's slices are written: one arrival at every owner,
+        // releasing the writes at cluster scope.
+#pragma unroll
+        for (int r = 0; r < CL; ++r) ptx::mbar_arrive_cluster(ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
+        if (!warp_wait<true>(W, rfull_bar, 0, kStatusTimeoutEpilogue)) break;
+#pragma unroll
+        for (int cg = 0; cg < kOwnCols / 32; ++cg) {
+          float4 acc[8];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) acc[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < CL; ++j)
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 t = ld_shared_v4(smem_base + j * kSlotBytes + ((cg * 8 + c4) * kBM + row) * 16);
+              acc[c4].x += t.x;
+              acc[c4].y += t.y;
+              acc[c4].z += t.z;
+              acc[c4].w += t.w;
+            }
+          uint32_t hs[16];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            hs[2 * c4] = pack_half2(acc[c4].x, acc[c4].y);
+            hs[2 * c4 + 1] = pack_half2(acc[c4].z, acc[c4].w);
+          }
+          if (rows_live) store_box(x, crank * kOwnCols + 32 * cg, hs);
         }
         continue;
       }
@@ -643,9 +742,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 }
 
 // ---------------------------------------------------------------- launcher
-template <int BN, int CL, bool P2 = false>
+template <int BN, int CL, int MODE>
 static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream, bool pdl) {
-  using Cfg = TileCfg<BN, P2>;
+  using Cfg = TileCfg<BN, MODE == kModePair>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
@@ -670,22 +769,22 @@ static cudaError_t launch_bn(const GemmParams& p, int grid, cudaStream_t stream,
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, CL, P2>, p);
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<BN, CL, MODE>, p);
 }
 
-template <int BN, int CL, bool P2 = false>
+template <int BN, int CL, int MODE>
 static cudaError_t prepare_bn() {
-  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, CL, P2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TileCfg<BN, P2>::kDynSmem);
+  return cudaFuncSetAttribute(nvfp4_gemm_kernel<BN, CL, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TileCfg<BN, MODE == kModePair>::kDynSmem);
 }
 
 // Largest number of co-resident clusters of CL CTAs (0 on error).
-template <int BN, int CL, bool P2 = false>
+template <int BN, int CL, int MODE>
 static int max_clusters_bn() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL * 1024, 1, 1);
   cfg.blockDim = dim3(kNumThreads, 1, 1);
-  cfg.dynamicSmemBytes = TileCfg<BN, P2>::kDynSmem;
+  cfg.dynamicSmemBytes = TileCfg<BN, MODE == kModePair>::kDynSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
@@ -694,47 +793,71 @@ static int max_clusters_bn() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<BN, CL, P2>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<BN, CL, MODE>, &cfg) != cudaSuccess) return 0;
   return n;
 }
 
 cudaError_t gemm_prepare_device(int bn) {
   cudaError_t e;
   switch (bn) {
-    case 64: return prepare_bn<64, 1>();
+    case 64: return prepare_bn<64, 1, kModeSingle>();
     case 128:
-      if ((e = prepare_bn<128, 1>()) != cudaSuccess) return e;
-      return prepare_bn<128, 2>();
+      if ((e = prepare_bn<128, 1, kModeSingle>()) != cudaSuccess) return e;
+      if ((e = prepare_bn<128, 2, kModeMulticast>()) != cudaSuccess) return e;
+      if ((e = prepare_bn<128, 2, kModeReduce>()) != cudaSuccess) return e;
+      return prepare_bn<128, 4, kModeReduce>();
     case 256:
-      if ((e = prepare_bn<256, 1>()) != cudaSuccess) return e;
-      if ((e = prepare_bn<256, 2>()) != cudaSuccess) return e;
-      return prepare_bn<256, 2, true>();
+      if ((e = prepare_bn<256, 1, kModeSingle>()) != cudaSuccess) return e;
+      if ((e = prepare_bn<256, 2, kModeMulticast>()) != cudaSuccess) return e;
+      return prepare_bn<256, 2, kModePair>();
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t gemm_launch(int bn, int cluster, bool pair, const GemmParams& p, int grid, cudaStream_t stream,
+// Launch of the variant for (BN, mode, cluster size); cudaErrorInvalidValue for
+// combinations that are not instantiated.
+cudaError_t gemm_launch(int bn, int cluster, int mode, const GemmParams& p, int grid, cudaStream_t stream,
                         bool pdl) {
-  if (pair) return (cluster == 2 && bn == 256) ? launch_bn<256, 2, true>(p, grid, stream, pdl) : cudaErrorInvalidValue;
-  if (cluster == 2) {
-    switch (bn) {
-      case 128: return launch_bn<128, 2>(p, grid, stream, pdl);
-      case 256: return launch_bn<256, 2>(p, grid, stream, pdl);
-      default: return cudaErrorInvalidValue;
-    }
+  switch (mode) {
+    case kModeSingle:
+      if (cluster != 1) break;
+      switch (bn) {
+        case 64: return launch_bn<64, 1, kModeSingle>(p, grid, stream, pdl);
+        case 128: return launch_bn<128, 1, kModeSingle>(p, grid, stream, pdl);
+        case 256: return launch_bn<256, 1, kModeSingle>(p, grid, stream, pdl);
+        default: break;
+      }
+      break;
+    case kModeMulticast:
+      if (cluster != 2) break;
+      if (bn == 128) return launch_bn<128, 2, kModeMulticast>(p, grid, stream, pdl);
+      if (bn == 256) return launch_bn<256, 2, kModeMulticast>(p, grid, stream, pdl);
+      break;
+    case kModePair:
+      if (cluster == 2 && bn == 256) return launch_bn<256, 2, kModePair>(p, grid, stream, pdl);
+      break;
+    case kModeReduce:
+      if (bn != 128) break;
+      if (cluster == 2) return launch_bn<128, 2, kModeReduce>(p, grid, stream, pdl);
+      if (cluster == 4) return launch_bn<128, 4, kModeReduce>(p, grid, stream, pdl);
+      break;
+    default: break;
   }
-  switch (bn) {
-    case 64: return launch_bn<64, 1>(p, grid, stream, pdl);
-    case 128: return launch_bn<128, 1>(p, grid, stream, pdl);
-    case 256: return launch_bn<256, 1>(p, grid, stream, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  return cudaErrorInvalidValue;
 }
 
-int gemm_max_clusters(int bn, int cluster, bool pair) {
-  if (cluster != 2) return 0;
-  if (pair) return bn == 256 ? max_clusters_bn<256, 2, true>() : 0;
-  return bn == 256 ? max_clusters_bn<256, 2>() : max_clusters_bn<128, 2>();
+int gemm_max_clusters(int bn, int cluster, int mode) {
+  switch (mode) {
+    case kModeMulticast:
+      if (cluster != 2) return 0;
+      return bn == 256 ? max_clusters_bn<256, 2, kModeMulticast>() : bn == 128 ? max_clusters_bn<128, 2, kModeMulticast>() : 0;
+    case kModePair:
+      return (cluster == 2 && bn == 256) ? max_clusters_bn<256, 2, kModePair>() : 0;
+    case kModeReduce:
+      if (bn != 128) return 0;
+      return cluster == 2 ? max_clusters_bn<128, 2, kModeReduce>() : cluster == 4 ? max_clusters_bn<128, 4, kModeReduce>() : 0;
+    default: return 0;
+  }
 }
 
 int gemm_stages(int bn, bool pair) {

@@ -35,6 +35,18 @@ constexpr int kNumThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
 constexpr int kStatusTimeoutProducer = 1;
 constexpr int kStatusTimeoutMma = 2;
 constexpr int kStatusTimeoutEpilogue = 3;
+constexpr int kStatusBadClusterPlan = 4;  // cluster reduction launched on a plan it does not fit
+
+// Kernel variants (template MODE; CL = CTAs per cluster):
+//   kModeSingle     CL = 1, one CTA per tile
+//   kModeMulticast  CL = 2, tiles 2q, 2q+1 of the same B columns share B by TMA multicast
+//   kModePair       CL = 2, the same two tiles as one 256-row tile of 2-SM MMAs
+//   kModeReduce     CL = S, the S stream-K segments of one tile, summed through
+//                   distributed shared memory instead of a global workspace
+constexpr int kModeSingle = 0;
+constexpr int kModeMulticast = 1;
+constexpr int kModePair = 2;
+constexpr int kModeReduce = 3;
 
 // Host-built parameter block, passed by value as a __grid_constant__ kernel
 // parameter: the tensor maps live in the parameter space and need no device

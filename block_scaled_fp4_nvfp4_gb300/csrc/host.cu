@@ -29,9 +29,9 @@
 
 namespace nvfp4 {
 cudaError_t gemm_prepare_device(int bn);
-cudaError_t gemm_launch(int bn, int cluster, bool pair, const GemmParams& p, int grid, cudaStream_t stream,
+cudaError_t gemm_launch(int bn, int cluster, int mode, const GemmParams& p, int grid, cudaStream_t stream,
                         bool pdl);
-int gemm_max_clusters(int bn, int cluster, bool pair);
+int gemm_max_clusters(int bn, int cluster, int mode);
 int gemm_stages(int bn, bool pair);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
 }  // namespace nvfp4
@@ -41,6 +41,8 @@ using namespace nvfp4;
 namespace {
 
 thread_local std::string g_last_error;
+// The calling thread's last GEMM launch: BN, grid, cluster, variant, stages.
+thread_local int g_last_launch[5] = {0, 0, 0, -1, 0};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -71,7 +73,9 @@ struct DeviceState {
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;       // device status word
   bool prepared_bn[3] = {false, false, false};  // BN = 128, 256, 64
-  int max_clusters[3] = {0, 0, 0};       // co-resident 2-CTA clusters: BN = 128, 256, 2-SM pairs
+  // co-resident clusters per variant: multicast BN = 128, 256; 2-SM pairs;
+  // cluster reduction with 2 and 4 CTAs
+  int max_clusters[5] = {0, 0, 0, 0, 0};
 };
 
 struct Workspace {
@@ -224,6 +228,7 @@ struct Plan {
   int bn = 128;
   int cluster = 1;  // CTAs per cluster (2: pairs sharing B tiles)
   bool pair = false;  // cluster == 2 as one 256-row tile of 2-SM MMAs (else B multicast)
+  bool red = false;   // stream-K segments of a tile as one cluster, reduced in shared memory
   int stages = 0;
   int grid = 0;     // CTAs
   int tiles_m[kMaxGroups] = {}, tiles_n[kMaxGroups] = {};
@@ -309,8 +314,19 @@ bool choose_pair(int cluster, int bn) {
   return true;
 }
 
+// Cluster reduction (NVFP4_SKRED = 0 disables): a stream-K plan whose CTAs
+// each run exactly one of S equal segments of a tile (S = 2 or 4, 128-wide
+// tiles) launches the S segments of each tile as one cluster; they exchange
+// their fp32 partials through distributed shared memory and each stores
+// 128/S columns, so no workspace, counters or last-arriver pass are needed.
+bool red_allowed() {
+  if (const char* env = getenv("NVFP4_SKRED")) return atoi(env) != 0;
+  return true;
+}
+
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl,
               bool allow_cluster = true) {
+  pl->red = false;
   pl->bn = choose_bn(G, M, N, L, sms);
   Schedule& s = pl->sched;
   memset(&s, 0, sizeof s);
@@ -388,6 +404,13 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     s.sk_max_segs = max_segs;
     pl->counters = static_cast<int>(tiles - dp);
     pl->workspace_bytes = max_segs > 1 ? static_cast<size_t>(tiles - dp) * max_segs * kBM * pl->bn * sizeof(float) : 0;
+    const long long S = pl->grid / tiles;
+    if (allow_cluster && mode == kSchedAuto && dp == 0 && pl->bn == 128 && (S == 2 || S == 4) &&
+        pl->grid == tiles * S && max_segs == S && red_allowed()) {
+      pl->red = true;
+      pl->counters = 0;
+      pl->workspace_bytes = 0;
+    }
   } else {
     pl->grid = static_cast<int>(tiles < sms ? tiles : sms);
     s.sk_max_segs = 1;
@@ -396,16 +419,22 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
   }
   if (pl->grid < 1) pl->grid = 1;
   s.cluster = 1;
-  pl->cluster = choose_cluster(s, sms, allow_cluster, pl->bn);
-  if (pl->cluster > 1) {
+  pl->cluster = pl->red ? static_cast<int>(pl->grid / s.total_tiles) : choose_cluster(s, sms, allow_cluster, pl->bn);
+  if (pl->cluster > 1 && !pl->red) {
     s.cluster = pl->cluster;
     const long long groups = tiles / pl->cluster;
     const long long per_wave = sms / pl->cluster;
     pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * pl->cluster);
   }
-  pl->pair = choose_pair(pl->cluster, pl->bn);
+  pl->pair = !pl->red && choose_pair(pl->cluster, pl->bn);
   pl->stages = gemm_stages(pl->bn, pl->pair);
   return NVFP4_OK;
+}
+
+int launch_mode(const Plan& pl) {
+  if (pl.red) return kModeReduce;
+  if (pl.pair) return kModePair;
+  return pl.cluster == 2 ? kModeMulticast : kModeSingle;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -507,31 +536,34 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
 
   Plan pl;
   if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
-  if (pl.cluster > 1) {
-    // persistent grid: no more clusters than can be co-resident
-    const int bi = pl.pair ? 2 : pl.bn == 256 ? 1 : 0;
-    if (ds->max_clusters[bi] == 0) ds->max_clusters[bi] = gemm_max_clusters(pl.bn, pl.cluster, pl.pair);
-    const int mc = ds->max_clusters[bi];
-    if (mc < 1) {
-      pl.cluster = 1;
-      pl.pair = false;
-      pl.sched.cluster = 1;
-      pl.grid = pl.sched.total_tiles < ds->sms ? pl.sched.total_tiles : ds->sms;
-    } else if (pl.grid / pl.cluster > mc) {
-      pl.grid = mc * pl.cluster;
-    }
-  }
+  // Shared-memory attributes of every variant of this tile width first: the
+  // occupancy query below needs them.
   const int bn_i = pl.bn == 256 ? 1 : pl.bn == 64 ? 2 : 0;
   if (!ds->prepared_bn[bn_i]) {
     if ((e = gemm_prepare_device(pl.bn)) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     ds->prepared_bn[bn_i] = true;
+  }
+  if (pl.cluster > 1) {
+    const int bi = pl.red ? (pl.cluster == 2 ? 3 : 4) : pl.pair ? 2 : pl.bn == 256 ? 1 : 0;
+    if (ds->max_clusters[bi] == 0) ds->max_clusters[bi] = gemm_max_clusters(pl.bn, pl.cluster, launch_mode(pl));
+    const int mc = ds->max_clusters[bi];
+    if (mc < 1) {
+      // this device cannot hold such a cluster: plan again without clusters
+      if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl, /*allow_cluster=*/false)) != NVFP4_OK) return rc;
+    } else if (!pl.red && pl.grid / pl.cluster > mc) {
+      // persistent grid: no more clusters than can be co-resident (a reduction
+      // cluster runs one tile and waits on no other cluster, so it needs none)
+      pl.grid = mc * pl.cluster;
+    }
   }
 
   GemmParams p;
   memset(&p, 0, sizeof p);
   for (int g = 0; g < G; ++g) {
     if ((rc = encode_operand_map(&p.tmA[g], A[g], M[g], K[g], L[g], kBM)) != NVFP4_OK) return rc;
-    if ((rc = encode_operand_map(&p.tmB[g], B[g], N[g], K[g], L[g], pl.bn / pl.cluster)) != NVFP4_OK) return rc;
+    // CTAs sharing B tiles (multicast, pair) each load half of the tile's rows
+    const int b_rows = (pl.cluster == 2 && !pl.red) ? pl.bn / 2 : pl.bn;
+    if ((rc = encode_operand_map(&p.tmB[g], B[g], N[g], K[g], L[g], b_rows)) != NVFP4_OK) return rc;
     if ((rc = encode_c_map(&p.tmC[g], C[g], M[g], N[g], L[g])) != NVFP4_OK) return rc;
     p.sfa[g] = static_cast<const uint8_t*>(SFA[g]);
     p.sfb[g] = static_cast<const uint8_t*>(SFB[g]);
@@ -562,8 +594,13 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
     p.counters = w->counters;
   }
 
-  e = gemm_launch(pl.bn, pl.cluster, pl.pair, p, pl.grid, stream, true);
+  e = gemm_launch(pl.bn, pl.cluster, launch_mode(pl), p, pl.grid, stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  g_last_launch[0] = pl.bn;
+  g_last_launch[1] = pl.grid;
+  g_last_launch[2] = pl.cluster;
+  g_last_launch[3] = launch_mode(pl);
+  g_last_launch[4] = gemm_stages(pl.bn, pl.pair);
   return ok();
 }
 
@@ -634,6 +671,7 @@ int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* 
   out[7] = pl.sched.sk_max_segs;
   if (out_len >= 9) out[8] = pl.cluster;
   if (out_len >= 10) out[9] = pl.pair ? 1 : 0;
+  if (out_len >= 11) out[10] = pl.red ? 1 : 0;
   return ok();
 }
 
@@ -646,8 +684,8 @@ int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K, c
   if ((rc = make_plan(G, M, N, K, L, num_sms, &pl)) != NVFP4_OK) return rc;
   if (cta < 0 || cta >= pl.grid) return fail(NVFP4_ERR_INVALID_ARG, "cta %d outside the grid of %d", cta, pl.grid);
   WorkCursor cur;
-  const int unit = cta / pl.cluster, units = pl.grid / pl.cluster;
-  work_begin(pl.sched, unit, units, cur, cta % pl.cluster);
+  const int unit = pl.red ? cta : cta / pl.cluster, units = pl.red ? pl.grid : pl.grid / pl.cluster;
+  work_begin(pl.sched, unit, units, cur, pl.red ? 0 : cta % pl.cluster);
   Work w;
   int n = 0;
   while (work_next(pl.sched, unit, units, cur, w)) {
@@ -660,6 +698,12 @@ int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K, c
   }
   g_last_error.clear();
   return n;
+}
+
+int nvfp4_gemm_last_launch(int* out, int out_len) {
+  if (!out || out_len < 1) return fail(NVFP4_ERR_INVALID_ARG, "bad output array");
+  for (int i = 0; i < out_len && i < 5; ++i) out[i] = g_last_launch[i];
+  return ok();
 }
 
 uint32_t nvfp4_gemm_encode_idesc(int M, int N) { return make_idesc_nvf4(M, N); }
@@ -779,7 +823,12 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   const size_t clear = kNoAllocHeader + static_cast<size_t>(pl.counters) * sizeof(int);
   if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
-  e = gemm_launch(pl.bn, 1, false, p, pl.grid, stream, false);  // follows a memset: plain launch
+  e = gemm_launch(pl.bn, 1, kModeSingle, p, pl.grid, stream, false);  // follows a memset: plain launch
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  g_last_launch[0] = pl.bn;
+  g_last_launch[1] = pl.grid;
+  g_last_launch[2] = 1;
+  g_last_launch[3] = kModeSingle;
+  g_last_launch[4] = gemm_stages(pl.bn, false);
   return ok();
 }

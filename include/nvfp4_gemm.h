@@ -159,6 +159,9 @@ NVFP4_API int nvfp4_gemm_debug_inject_skip(int ktile);
  *   out[9] (when out_len >= 10) 1 when such a pair runs as one 256 x BN tile of
  *          2-SM MMAs (tcgen05 cta_group::2, each CTA holding half of B), 0 when
  *          the pair shares B through cluster multicast
+ *   out[10] (when out_len >= 11) 1 when the stream-K segments of each tile run
+ *          as one cluster (out[8] CTAs, one segment each) and are summed in
+ *          distributed shared memory instead of a device workspace
  */
 NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, const int* L,
                     int num_sms, int* out, int out_len);
@@ -172,6 +175,19 @@ NVFP4_API int nvfp4_gemm_plan(int G, const int* M, const int* N, const int* K, c
  */
 NVFP4_API int nvfp4_gemm_debug_schedule(int G, const int* M, const int* N, const int* K,
                                         const int* L, int num_sms, int cta, int* out, int out_cap);
+
+/*
+ * What the calling host thread's most recent successful GEMM launch
+ * (nvfp4_gemm_run, _run_grouped or _run_noalloc) actually ran, after any
+ * device-dependent fallback of the plan.  Writes min(out_len, 5) ints:
+ *   out[0] BN    out[1] grid (CTAs)    out[2] CTAs per cluster
+ *   out[3] variant: 0 one CTA per tile, 1 CTA pairs sharing B by multicast,
+ *          2 CTA pairs running 2-SM MMAs, 3 stream-K segments reduced in a
+ *          cluster's distributed shared memory; -1 before the first launch
+ *   out[4] shared-memory stages
+ * Host only, no device call.  Errors: INVALID_ARG (null out, out_len < 1).
+ */
+NVFP4_API int nvfp4_gemm_last_launch(int* out, int out_len);
 
 /*
  * nvfp4_gemm_run without any device allocation.  The source pages have no

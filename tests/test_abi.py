@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = binding.header_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     for n in names:
         assert hasattr(lib, n), n
         ctypes.cast(getattr(lib, n), ctypes.c_void_p)
@@ -205,6 +205,14 @@ def test_pointer_errors_without_gpu(lib):
     assert e.value.code == -1
 
 
+def test_last_launch_before_any_launch(lib):
+    info = binding.nvfp4_gemm_last_launch()
+    assert info["variant"] is None or info["variant"] in ("single", "multicast", "pair", "cluster_reduce")
+    with pytest.raises(binding.Nvfp4Error):
+        _check_rc = lib.nvfp4_gemm_last_launch(None, 5)
+        binding._check(_check_rc, "nvfp4_gemm_last_launch")
+
+
 def test_timeout_setting_validated(lib):
     with pytest.raises(binding.Nvfp4Error):
         binding.nvfp4_gemm_set_wait_timeout_ns(10)
@@ -227,7 +235,8 @@ def test_cluster_pairs_share_b_columns(lib, monkeypatch):
                 assert b["tm"] == a["tm"] + 1 and a["tm"] % 2 == 0
     # odd m-tile counts, stream-K plans and the override fall back to single CTAs
     assert binding.nvfp4_gemm_plan([384, 64], [4096, 4096], [7168, 7168], [1, 1], 152)["cluster"] == 1
-    assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["cluster"] == 1
+    p = binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)   # stream-K: clusters only for the reduction
+    assert p["pair"] == 0 and (p["cluster"] == 1 or p["cluster_reduce"] == 1)
     monkeypatch.setenv("NVFP4_CLUSTER", "1")
     assert binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)["cluster"] == 1
     monkeypatch.setenv("NVFP4_CLUSTER", "2")
@@ -250,3 +259,29 @@ def test_pair_tiles_planned_for_wide_clusters(lib, monkeypatch):
     assert p["cluster"] == 2 and p["pair"] == 0
     monkeypatch.delenv("NVFP4_BN")
     assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["pair"] == 0
+
+
+def test_cluster_reduction_planned_for_one_segment_per_cta(lib, monkeypatch):
+    """Stream-K plans whose CTAs each run one of S = 2 or 4 equal segments
+    launch each tile's segments as one cluster (rank = segment) and need no
+    workspace; other plans keep the workspace path."""
+    p = binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)
+    assert p["cluster_reduce"] == 1 and p["cluster"] == 2 and p["grid"] == 112
+    p4 = binding.nvfp4_gemm_plan([128], [512], [4096], [1], 152)
+    assert p4["cluster_reduce"] == 1 and p4["cluster"] == 4 and p4["grid"] == 16
+    for M, N, K, L in (([128], [7168], [16384], [1]), ([128], [512], [4096], [1]), ([300], [264], [1024], [2])):
+        p = binding.nvfp4_gemm_plan(M, N, K, L, 152)
+        if not p["cluster_reduce"]:
+            continue
+        S = p["cluster"]
+        for cta in range(p["grid"]):
+            (w,) = binding.nvfp4_gemm_debug_schedule(M, N, K, L, 152, cta)
+            assert w["nseg"] == S and w["seg"] == cta % S and w["tile"] == cta // S
+        _check_schedule(M, N, K, L, 152)
+    assert binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)["cluster_reduce"] == 0
+    monkeypatch.setenv("NVFP4_SKRED", "0")
+    p = binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)
+    assert p["cluster_reduce"] == 0 and p["cluster"] == 1 and p["grid"] == 112
+    monkeypatch.setenv("NVFP4_SKRED", "1")
+    monkeypatch.setenv("NVFP4_SCHEDULE", "sk")   # uneven ranges: workspace path
+    assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["cluster_reduce"] == 0

@@ -78,6 +78,8 @@ def test_one_hot_scales_pin_the_atom_layout(config, monkeypatch):
         d = to_device(p)
         _, C = alloc_c(M, N, 1)
         run_single(d, C)
+        if config == "pair":
+            assert binding.nvfp4_gemm_last_launch()["variant"] == "pair"
         binding.nvfp4_gemm_check_device_status()
         assert_close_full(C, p)
 
@@ -228,6 +230,7 @@ def test_parity_cluster_pairs(bn, M, N, K, L, monkeypatch):
     d = to_device(p)
     buf, C = alloc_c(M, N, L)
     run_single(d, C)
+    assert binding.nvfp4_gemm_last_launch()["variant"] in ("multicast", "pair")
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, L)
@@ -252,6 +255,7 @@ def test_parity_pair_tiles(pair, M, N, K, L, monkeypatch):
     d = to_device(p)
     buf, C = alloc_c(M, N, L)
     run_single(d, C)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == ("pair" if pair == "1" else "multicast")
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, L)
@@ -273,6 +277,7 @@ def test_parity_pair_tiles_grouped(monkeypatch):
     Cs = [alloc_c(Ms[g], Ns[g], 1) for g in range(3)]
     binding.nvfp4_gemm_run_grouped(3, [d["A"] for d in ds], [d["B"] for d in ds], [d["SFA"] for d in ds],
                                    [d["SFB"] for d in ds], [c[1] for c in Cs], Ms, Ns, Ks, [1] * 3)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == "pair"
     binding.nvfp4_gemm_check_device_status()
     for g in range(3):
         assert_close_full(Cs[g][1], probs[g])
@@ -366,6 +371,68 @@ def test_parity_partial_k_tiles_pairs(pair, M, N, K, monkeypatch):
     assert plan["cluster"] == 2 and plan["pair"] == int(pair)
     p = workloads.make_random_problem(M + 7 * N + K, M, N, K, 1)
     d = to_device(p)
+    buf, C = alloc_c(M, N, 1)
+    run_single(d, C)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == ("pair" if pair == "1" else "multicast")
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, 1)
+
+
+@pytest.mark.parametrize("M,N,K,L", [(128, 7168, 16384, 1), (128, 512, 4096, 1), (100, 1032, 2048, 1),
+                                     (64, 2048, 4096, 1), (200, 264, 2048, 2), (128, 3072, 1984, 1)])
+def test_cluster_reduction_matches_workspace_path(M, N, K, L, monkeypatch):
+    """Stream-K segments summed in distributed shared memory (clusters of 2 or
+    4 CTAs) give the same bits as the workspace path (same k-order sums),
+    and both match the oracle."""
+    binding = require_gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    monkeypatch.delenv("NVFP4_SKRED", raising=False)
+    plan = binding.nvfp4_gemm_plan([M], [N], [K], [L], sms)
+    assert plan["cluster_reduce"] == 1, plan
+    p = workloads.make_random_problem(M * 3 + N + K * 5 + L, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    launched = binding.nvfp4_gemm_last_launch()
+    assert launched["variant"] == "cluster_reduce" and launched["cluster"] == plan["cluster"]
+    binding.nvfp4_gemm_check_device_status()
+    check_canary(buf, M, N, L)
+    monkeypatch.setenv("NVFP4_SKRED", "0")
+    assert binding.nvfp4_gemm_plan([M], [N], [K], [L], sms)["cluster_reduce"] == 0
+    buf2, C2 = alloc_c(M, N, L)
+    run_single(d, C2)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == "single"
+    binding.nvfp4_gemm_check_device_status()
+    assert torch.equal(C.view(torch.int16), C2.view(torch.int16))
+    if M * N * K <= 128 * 7168 * 4096:
+        assert_close_full(C, p)
+    else:
+        ls, ms, ns = sample_points(M, N, L, 3000, seed=9)
+        assert_close_points(C, p, ls, ms, ns)
+
+
+def test_cluster_reduction_timeout_is_reported(monkeypatch):
+    """A skipped k-tile in one segment of a reduction cluster: every CTA of the
+    cluster gives up, the host sees the timeout, and the next call is right."""
+    binding = require_gpu()
+    monkeypatch.delenv("NVFP4_SKRED", raising=False)
+    M, N, K = 128, 512, 4096
+    assert binding.nvfp4_gemm_plan([M], [N], [K], [1], torch.cuda.get_device_properties(0).multi_processor_count)[
+        "cluster_reduce"] == 1
+    p = workloads.make_random_problem(17, M, N, K)
+    d = to_device(p)
+    try:
+        binding.nvfp4_gemm_set_wait_timeout_ns(50_000_000)
+        binding.nvfp4_gemm_debug_inject_skip(1)
+        _, C = alloc_c(M, N, 1)
+        run_single(d, C)
+        with pytest.raises(binding.Nvfp4Error) as e:
+            binding.nvfp4_gemm_check_device_status()
+        assert e.value.code == -4
+    finally:
+        binding.nvfp4_gemm_debug_inject_skip(-1)
+        binding.nvfp4_gemm_set_wait_timeout_ns(2_000_000_000)
     buf, C = alloc_c(M, N, 1)
     run_single(d, C)
     binding.nvfp4_gemm_check_device_status()
