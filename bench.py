@@ -43,7 +43,7 @@ METRIC = "NVFP4 (grouped) GEMM TFLOPS, device-timed, and % of FP4-tensor/HBM roo
 DEFAULT_WORKLOAD = "skinny_128x7168x16384"
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio, used to scale the measured bf16 peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["gemm_kernel.cu", "gemm_params.h", "ptx.cuh", "descriptors.h"]
+KERNEL_SOURCES = ["gemm_kernel.cu", "gemm_params.h", "ptx.cuh", "descriptors.h", "schedule.h"]
 
 
 def parse():
