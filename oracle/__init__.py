@@ -13,7 +13,9 @@ Pins (tests marked ``not gpu``): decode tables against the format's published
 value list and ``torch.float8_e4m3fn``; tiny GEMMs against exact rational
 arithmetic; unit scales against the plain decoded matmul; grouped output against
 single-problem runs; fp64->fp16 rounding by brute force; the repack layout
-against the pages' logical shape and address arithmetic.
+against the pages' logical shape and address arithmetic; the NVFP4 quantizer's
+encoders against the decode tables (exact round trips, midpoints to the even
+code, saturation) and ``torch.float8_e4m3fn``, and a hand-worked block.
 """
 import ctypes
 import os
@@ -55,6 +57,11 @@ def _load():
         lib.oracle_repack_scales.argtypes = [u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p]
         lib.oracle_repack_scales.restype = ctypes.c_int
         lib.oracle_max_threads.restype = ctypes.c_int
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_e4m3_encode_array.argtypes = [fp, u8p, ctypes.c_int64]
+        lib.oracle_e2m1_encode_array.argtypes = [fp, u8p, ctypes.c_int64]
+        lib.oracle_quantize.argtypes = [fp, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
+        lib.oracle_quantize.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -184,6 +191,40 @@ def repack_scales(sf, rows, K, L=1) -> np.ndarray:
     if rc != 0:
         raise RuntimeError("oracle_repack_scales failed: %d" % rc)
     return out
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """fp32 -> E4M3 code (RNE, ties to the even code, finite values above 448 -> 448)."""
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    out = np.zeros(a.shape, np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(a, ctypes.c_float), _ptr(out, ctypes.c_uint8), a.size)
+    return out
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """fp32 -> E2M1 code (RNE on the value grid, ties to the even code,
+    magnitudes above 6 -> 6, sign bit = sign bit of v)."""
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    out = np.zeros(a.shape, np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(a, ctypes.c_float), _ptr(out, ctypes.c_uint8), a.size)
+    return out
+
+
+def quantize(x, rows, K, L=1):
+    """x [L, rows, K] (float32, or a bf16/fp16 torch tensor: converted exactly)
+    -> (codes u8 [L, rows, K/2], row-major scales u8 [L, rows, K/16]).
+    The recipe is stated in nvfp4_oracle.c (amax/6 as E4M3, codes RNE)."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().float().contiguous().numpy()
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    assert x.size == L * rows * K and K % 16 == 0
+    codes = np.zeros((L, rows, K // 2), np.uint8)
+    sf = np.zeros((L, rows, K // 16), np.uint8)
+    rc = _load().oracle_quantize(_ptr(x, ctypes.c_float), rows, K, L, _ptr(codes, ctypes.c_uint8),
+                                 _ptr(sf, ctypes.c_uint8))
+    if rc != 0:
+        raise RuntimeError("oracle_quantize failed: %d" % rc)
+    return codes, sf
 
 
 def tolerance(ref_f16, absacc):

@@ -347,6 +347,95 @@ int oracle_repack_scales(const uint8_t* sf, int rows, int K, int L, uint8_t* out
     return 0;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Quantization to NVFP4: the step that produces A, B and their scales.       */
+/*                                                                            */
+/* The pages take A, B, SFA and SFB already quantized (the harness generates  */
+/* them) and print no quantizer, so this is the plainest reading of the       */
+/* formats they name (E2M1 codes, one E4M3 scale per 16 consecutive k),       */
+/* stated in IEEE fp32 on both the oracle and the GPU side:                   */
+/*   amax    = max |x_i| over the 16 values of a block                        */
+/*   sf      = E4M3(amax / 6)    6 = largest E2M1 magnitude; round to nearest, */
+/*                               ties to the even code; finite values above    */
+/*                               448 give 448                                  */
+/*   d       = the value of sf                                                 */
+/*   code_i  = E2M1(x_i / d)     round to nearest on {0,.5,1,1.5,2,3,4,6},     */
+/*                               ties to the even code, magnitudes above 6     */
+/*                               give 6, sign bit = sign bit of x_i / d;       */
+/*                               d = 0 gives code 0                            */
+/* x / d and amax / 6 are single correctly rounded fp32 divisions.            */
+/* ------------------------------------------------------------------------- */
+
+/* Index of the table entry nearest to v >= 0 among codes 0..ncodes-1 (whose */
+/* values increase with the code), by plain scan; a tie goes to the even     */
+/* code.                                                                     */
+static unsigned nearest_code(double v, const double* tab, unsigned ncodes) {
+    unsigned best = 0;
+    double bd = fabs(v - tab[0]);
+    for (unsigned c = 1; c < ncodes; ++c) {
+        double d = fabs(v - tab[c]);
+        if (d < bd || (d == bd && (c & 1u) == 0 && (best & 1u) == 1)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return best;
+}
+
+uint8_t oracle_e4m3_encode(float v) {
+    build_tables();
+    if (isnan(v)) return 0x7F;
+    double a = fabs((double)v);
+    unsigned c = a >= 448.0 ? 0x7Eu : nearest_code(a, g_e4m3, 0x7F); /* finite codes 0x00..0x7E */
+    return (uint8_t)(c | (signbit(v) ? 0x80u : 0u));
+}
+
+uint8_t oracle_e2m1_encode(float v) {
+    build_tables();
+    double a = fabs((double)v);
+    unsigned c = a >= 6.0 ? 7u : nearest_code(a, g_e2m1, 8);
+    return (uint8_t)(c | (signbit(v) ? 8u : 0u));
+}
+
+void oracle_e4m3_encode_array(const float* v, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+void oracle_e2m1_encode_array(const float* v, uint8_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(v[i]);
+}
+
+/* x [L][rows][K] fp32 (the exact values of bf16 / fp16 inputs) -> codes      */
+/* [L][rows][K/2] (low nibble = even k) and row-major scales [L][rows][K/16]. */
+int oracle_quantize(const float* x, int rows, int K, int L, uint8_t* codes, uint8_t* sf) {
+    if (rows < 0 || K < 0 || L < 0 || (K % 16) != 0) return -1;
+    build_tables();
+    const int64_t nrow = (int64_t)L * rows;
+#pragma omp parallel for schedule(static)
+    for (int64_t lr = 0; lr < nrow; ++lr) {
+        const float* xr = x + lr * K;
+        uint8_t* cr = codes + lr * (K / 2);
+        uint8_t* sr = sf + lr * (K / 16);
+        for (int64_t b = 0; b < K / 16; ++b) {
+            float amax = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                float m = fabsf(xr[b * 16 + i]);
+                if (m > amax) amax = m;
+            }
+            const uint8_t sc = oracle_e4m3_encode(amax / 6.0f);
+            const float d = (float)g_e4m3[sc];
+            sr[b] = sc;
+            for (int i = 0; i < 16; i += 2) {
+                const float x0 = xr[b * 16 + i], x1 = xr[b * 16 + i + 1];
+                const uint8_t q0 = d == 0.0f ? 0 : oracle_e2m1_encode(x0 / d);
+                const uint8_t q1 = d == 0.0f ? 0 : oracle_e2m1_encode(x1 / d);
+                cr[(b * 16 + i) / 2] = (uint8_t)(q0 | (q1 << 4));
+            }
+        }
+    }
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
