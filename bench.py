@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--check", action="store_true", help="oracle check of set 0 (sampled)")
+    ap.add_argument("--no-quantize", action="store_true", help="skip the fused quantize + repack leg")
     return ap.parse_args()
 
 
@@ -381,6 +382,32 @@ def main():
     torch.cuda.synchronize()
     rp_ms = t0e.elapsed_time(t1e) / rp_steps
 
+    # ---- fused quantize + repack (the step that produces B and SFB) on a
+    # bf16 tensor shaped like group 0's B; larger than L2, so it streams HBM
+    quant = None
+    if not args.no_quantize:
+        q0 = host_sets[0][0]
+        qr, qk, ql = q0["N"], q0["K"], q0["L"]
+        gq = torch.Generator(device=dev).manual_seed(0)
+        xq = torch.randn((ql, qr, qk), device=dev, dtype=torch.float32, generator=gq).to(torch.bfloat16)
+        qcodes = torch.empty((ql, qr, qk // 2), dtype=torch.uint8, device=dev)
+        qsf = torch.empty(binding.nvfp4_gemm_repacked_scales_bytes(qr, qk, ql), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
+        torch.cuda.synchronize()
+        q_iters = 20
+        t0q, t1q = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0q.record(stream)
+        for _ in range(q_iters):
+            binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
+        t1q.record(stream)
+        torch.cuda.synchronize()
+        q_ms = t0q.elapsed_time(t1q) / q_iters
+        q_bytes = ql * qr * qk * 2 + ql * qr * qk // 2 + qsf.numel()
+        quant = {"shape_LxRxK": [ql, qr, qk], "input": "bf16", "us": q_ms * 1e3,
+                 "algorithmic_bytes": q_bytes, "achieved": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s"}
+        del xq, qcodes, qsf
+
     # ---- e2e: host buffers through the C ABI
     hp = []
     h2d = 0
@@ -471,6 +498,7 @@ def main():
                     "includes": "H2D of A, B, row-major SFA/SFB; 2 repacks; GEMM; D2H of C"},
             "step_with_repack": {"value": flops / (rp_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                                  "ms_per_step": rp_ms},
+            "quantize": None if quant is None else dict(quant, peak=hbm, frac=quant["achieved"] / hbm),
             "gpu_launches": args.steps,
             "clocks": clocks,
         }

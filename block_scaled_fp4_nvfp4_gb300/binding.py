@@ -69,6 +69,8 @@ def load_library(path=LIB_PATH):
     lib.nvfp4_gemm_plan.restype = i
     lib.nvfp4_gemm_debug_schedule.argtypes = [i, ip, ip, ip, ip, i, i, ip, i]
     lib.nvfp4_gemm_debug_schedule.restype = i
+    lib.nvfp4_quantize.argtypes = [vp, i, vp, vp, i, i, i, vp]
+    lib.nvfp4_quantize.restype = i
     lib.nvfp4_gemm_last_launch.argtypes = [ip, i]
     lib.nvfp4_gemm_last_launch.restype = i
     lib.nvfp4_gemm_encode_idesc.argtypes = [i, i]
@@ -83,7 +85,7 @@ def header_functions(path=HEADER_PATH):
     """Names of the functions declared in include/nvfp4_gemm.h."""
     text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(nvfp4_gemm_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", text)))
 
 
 def _ptr(x):
@@ -130,6 +132,16 @@ def nvfp4_gemm_run_noalloc(A, B, SFA, SFB, C, M, N, K, L=1, stream=None):
     rc = load_library().nvfp4_gemm_run_noalloc(_ptr(A), _ptr(B), _ptr(SFA), _ptr(SFB), _ptr(C), M, N, K,
                                                L, _stream(stream))
     _check(rc, "nvfp4_gemm_run_noalloc")
+
+
+DTYPE_BF16 = 0
+DTYPE_F16 = 1
+
+
+def nvfp4_quantize(x, x_dtype, codes, sf_repacked, rows, K, L=1, stream=None):
+    rc = load_library().nvfp4_quantize(_ptr(x), int(x_dtype), _ptr(codes), _ptr(sf_repacked), rows, K, L,
+                                       _stream(stream))
+    _check(rc, "nvfp4_quantize")
 
 
 def nvfp4_gemm_run_grouped(G, A, B, SFA, SFB, C, M, N, K, L, stream=None):
@@ -229,3 +241,18 @@ def gemm(A, B, SFA_rp, SFB_rp, M, N, K, L=1, C=None, stream=None):
         C = torch.empty((L, M, N), dtype=torch.float16, device=A.device)
     nvfp4_gemm_run(A, B, SFA_rp, SFB_rp, C, M, N, K, L, stream)
     return C
+
+
+def quantize(x, stream=None):
+    """x [L, rows, K] or [rows, K] bf16 / fp16 torch tensor on the GPU ->
+    (codes [L, rows, K/2] u8, repacked scales u8) via nvfp4_quantize."""
+    import torch
+    if x.dim() == 2:
+        x = x.unsqueeze(0)
+    L, rows, K = x.shape
+    dtype = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}[x.dtype]
+    x = x.contiguous()
+    codes = torch.empty((L, rows, K // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty(nvfp4_gemm_repacked_scales_bytes(rows, K, L), dtype=torch.uint8, device=x.device)
+    nvfp4_quantize(x, dtype, codes, sf, rows, K, L, stream)
+    return codes, sf

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4gemm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["host.cu", "gemm_kernel.cu", "repack.cu"]
+SOURCES = ["host.cu", "gemm_kernel.cu", "repack.cu", "quantize.cu"]
 HEADERS = ["gemm_params.h", "ptx.cuh", "descriptors.h", "schedule.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

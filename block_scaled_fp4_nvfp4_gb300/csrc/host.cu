@@ -34,6 +34,8 @@ cudaError_t gemm_launch(int bn, int cluster, int mode, const GemmParams& p, int 
 int gemm_max_clusters(int bn, int cluster, int mode);
 int gemm_stages(int bn, bool pair);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
+cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, int rows, int K, int L, int sms,
+                            cudaStream_t stream);
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -510,6 +512,30 @@ int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int K, int L, 
     return fail(NVFP4_ERR_INVALID_ARG, "bad sizes rows=%d K=%d L=%d (K %% 16 == 0 required)", rows, K, L);
   cudaError_t e = repack_launch(sf, out, rows, K, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+  return ok();
+}
+
+int nvfp4_quantize(const void* x, int x_dtype, void* codes, void* sf_repacked, int rows, int K, int L,
+                   void* stream) {
+  if (!x || !codes || !sf_repacked) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf_repacked))
+    return fail(NVFP4_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (x_dtype != NVFP4_DTYPE_BF16 && x_dtype != NVFP4_DTYPE_F16)
+    return fail(NVFP4_ERR_INVALID_ARG, "x_dtype %d is neither NVFP4_DTYPE_BF16 nor NVFP4_DTYPE_F16", x_dtype);
+  if (rows < 1 || K < 16 || L < 1 || K % 16 != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "bad sizes rows=%d K=%d L=%d (K %% 16 == 0 required)", rows, K, L);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState* ds = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int rc = device_state(dev, &ds);
+    if (rc != NVFP4_OK) return rc;
+  }
+  e = quantize_launch(x, x_dtype == NVFP4_DTYPE_F16, codes, sf_repacked, rows, K, L, ds->sms,
+                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return ok();
 }
 

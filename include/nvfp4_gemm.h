@@ -86,6 +86,33 @@ NVFP4_API size_t nvfp4_gemm_repacked_scales_bytes(int rows, int K, int L);
  */
 NVFP4_API int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int K, int L, void* stream);
 
+/* Input element types of nvfp4_quantize. */
+#define NVFP4_DTYPE_BF16 0
+#define NVFP4_DTYPE_F16 1
+
+/*
+ * Quantize values to NVFP4 and write the scales already repacked: the step
+ * that produces A (or B) and SFA (or SFB) for nvfp4_gemm_run.  The pages take
+ * pre-quantized inputs and print no quantizer; this is the plainest reading of
+ * the formats they name ("nvfp4 gemm, submission 125598": ab_dtype Float4E2M1FN,
+ * sf_dtype Float8E4M3FN, sf_vec_size 16), in IEEE fp32:
+ *   per 16 consecutive values along K:  sf = E4M3(amax / 6), round to nearest
+ *   even, finite values above 448 give 448;  d = value of sf;
+ *   code = E2M1(x / d), round to nearest even on {0, .5, 1, 1.5, 2, 3, 4, 6},
+ *   magnitudes above 6 give 6, sign of x / d kept;  d = 0 gives code 0.
+ *
+ *   x            device [L][rows][K], bf16 or fp16 per x_dtype, row-major
+ *   codes        device [L][rows][K/2] bytes, written (low nibble = even k)
+ *   sf_repacked  device, nvfp4_gemm_repacked_scales_bytes(rows, K, L) bytes,
+ *                written in full (padding rows and k-blocks as zero)
+ *   rows, K, L   rows >= 1, K >= 16 with K % 16 == 0, L >= 1
+ * Asynchronous on `stream`; pointers 16-byte aligned; x must not overlap the
+ * outputs.  Inputs with Inf or NaN are outside the contract.
+ * Errors: INVALID_ARG (null / misaligned pointer, sizes, dtype), CUDA.
+ */
+NVFP4_API int nvfp4_quantize(const void* x, int x_dtype, void* codes, void* sf_repacked, int rows, int K,
+                             int L, void* stream);
+
 /*
  * One problem: C = A * SFA * B * SFB ("nvfp4 gemm, submission 125598",
  * custom_kernel).  Equivalent to nvfp4_gemm_run_grouped with G = 1.

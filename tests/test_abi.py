@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = binding.header_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     for n in names:
         assert hasattr(lib, n), n
         ctypes.cast(getattr(lib, n), ctypes.c_void_p)
@@ -211,6 +211,17 @@ def test_last_launch_before_any_launch(lib):
     with pytest.raises(binding.Nvfp4Error):
         _check_rc = lib.nvfp4_gemm_last_launch(None, 5)
         binding._check(_check_rc, "nvfp4_gemm_last_launch")
+
+
+def test_quantize_argument_errors_without_gpu(lib):
+    for args in ((0, 0, 16, 16, 128, 256, 1),      # null x
+                 (16, 0, 16, 24, 128, 256, 1),     # misaligned scales
+                 (16, 2, 16, 16, 128, 256, 1),     # unknown dtype
+                 (16, 0, 16, 16, 128, 200, 1),     # K % 16
+                 (16, 1, 16, 16, 0, 256, 1)):      # rows
+        with pytest.raises(binding.Nvfp4Error) as e:
+            binding.nvfp4_quantize(*args, stream=0)
+        assert e.value.code == -1
 
 
 def test_timeout_setting_validated(lib):
