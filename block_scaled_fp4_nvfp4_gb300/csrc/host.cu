@@ -34,8 +34,9 @@ cudaError_t gemm_launch(int bn, int cluster, int mode, const GemmParams& p, int 
 int gemm_max_clusters(int bn, int cluster, int mode);
 int gemm_stages(int bn, bool pair);
 cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cudaStream_t stream);
-cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, int rows, int K, int L, int sms,
-                            cudaStream_t stream);
+cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, int rows, int K, int L,
+                            int max_blocks, cudaStream_t stream);
+int quantize_blocks_per_sm(int is_f16);
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -78,6 +79,7 @@ struct DeviceState {
   // co-resident clusters per variant: multicast BN = 128, 256; 2-SM pairs;
   // cluster reduction with 2 and 4 CTAs
   int max_clusters[5] = {0, 0, 0, 0, 0};
+  int quant_blocks_per_sm[2] = {0, 0};   // quantize kernel, bf16 / fp16 input
 };
 
 struct Workspace {
@@ -527,14 +529,18 @@ int nvfp4_quantize(const void* x, int x_dtype, void* codes, void* sf_repacked, i
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  DeviceState* ds = nullptr;
+  const int is_f16 = x_dtype == NVFP4_DTYPE_F16 ? 1 : 0;
+  int max_blocks = 0;
   {
     std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
     int rc = device_state(dev, &ds);
     if (rc != NVFP4_OK) return rc;
+    int& bps = ds->quant_blocks_per_sm[is_f16];
+    if (bps == 0) bps = quantize_blocks_per_sm(is_f16);
+    max_blocks = ds->sms * (bps > 0 ? bps : 1);
   }
-  e = quantize_launch(x, x_dtype == NVFP4_DTYPE_F16, codes, sf_repacked, rows, K, L, ds->sms,
-                      static_cast<cudaStream_t>(stream));
+  e = quantize_launch(x, is_f16, codes, sf_repacked, rows, K, L, max_blocks, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return ok();
 }

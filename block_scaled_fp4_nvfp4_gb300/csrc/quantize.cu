@@ -10,13 +10,25 @@
 //   code_i = E2M1(x_i / d), round to nearest even on {0, .5, 1, 1.5, 2, 3, 4, 6},
 //   magnitudes above 6 give 6, sign of x_i / d kept;  d = 0 gives code 0.
 //
-// Work split: one warp per (batch, 128-row block, 64-value chunk of K).  Lane i
-// owns rows 32q + i (q = 0..3) of the block: it reads each row's 64 values (one
-// 128-byte line), writes its 32 bytes of codes, and the 4 x 4 scale bytes it
-// produced form exactly its 16-byte row of the 512-byte scale atom (byte
-// (r % 32) * 16 + ((r % 128) / 32) * 4 + k-block % 4), so each warp writes one
-// whole atom with one 16-byte store per lane.  Atoms of the padding (rows past
-// the last row, k past K up to the 256-wide k-tile) are written as zeros.
+// Work split: one warp per (batch, 128-row block, 64-value chunk of K), i.e. per
+// 512-byte scale atom.  Eight lanes read one row's 128 bytes together (one full
+// line per 8 lanes, 512 contiguous bytes per warp load, 32 contiguous bytes of
+// codes per row per store); lanes 2b and 2b+1 hold 16-value block b and
+// combine their maxima with one shuffle.  The atom is assembled in shared
+// memory (byte (r % 32) * 16 + ((r % 128) / 32) * 4 + block % 4) and stored
+// with one 16-byte store per lane.  Atoms of the padding (rows past the last
+// row, k past K up to the 256-wide k-tile) come out zero.  The grid is one
+// wave of resident blocks walking the atoms.
+//
+// x / d without a full division per value: r = 1/d correctly rounded once per
+// block, q0 = RN(x r) (within one ulp of x / d), and Markstein's correction
+// step (P. Markstein, IBM J. Res. Develop. 34(1), 1990; Handbook of
+// Floating-Point Arithmetic, theorem on division with a correctly rounded
+// reciprocal) q = RN(q0 + RN(x - d q0) r), the remainder exact by FMA, is the
+// correctly rounded quotient when nothing underflows.  Values small enough to
+// underflow there are below a quarter of d and get code 0 whatever the
+// rounding.  The sign bit of each code is taken from the input's own sign bit,
+// so -0.0 keeps it.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -56,86 +68,108 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   }
 }
 
-// One block of 16 values: writes its 8 code bytes, returns its scale byte.
-template <bool kF16>
-__device__ __forceinline__ uint32_t quantize_block(const uint16_t* src, uint8_t* dst) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src);
-  const uint4 v0 = __ldcs(s4);
-  const uint4 v1 = __ldcs(s4 + 1);
-  float f[16];
-  unpack8<kF16>(v0, f);
-  unpack8<kF16>(v1, f + 8);
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
-  const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
-  uint32_t lo = 0, hi = 0;
-  if (d != 0.0f) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      lo |= e2m1x2(__fdiv_rn(f[2 * i], d), __fdiv_rn(f[2 * i + 1], d)) << (8 * i);
-      hi |= e2m1x2(__fdiv_rn(f[8 + 2 * i], d), __fdiv_rn(f[8 + 2 * i + 1], d)) << (8 * i);
-    }
-  }
-  *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-  return static_cast<uint32_t>(sc);
-}
+constexpr int kRowGroupsPerBatch = 4;  // groups of 4 rows loaded before any is processed
+constexpr int kThreads = 256;
 
 template <bool kF16>
-__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ codes,
-                                                       uint8_t* __restrict__ sf, int rows, int K, int L,
-                                                       int row_blocks, int atoms_per_block) {
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __restrict__ x,
+                                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                            int rows, int K, int L, int row_blocks,
+                                                            int atoms_per_block) {
+  __shared__ __align__(16) uint8_t atoms[kThreads / 32][512];  // one scale atom per warp
   const int lane = threadIdx.x & 31;
+  uint8_t* atom = atoms[threadIdx.x >> 5];
+  const int sub = lane >> 3;  // row of a group of 4 rows
+  const int j = lane & 7;     // 16-byte chunk (8 values) of the row's 64 values
+  const int b = j >> 1;       // 16-value block of the chunk
   const long long tasks = static_cast<long long>(L) * row_blocks * atoms_per_block;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int kblocks = K / 16;
   for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < tasks;
        t += nwarps) {
-    const int kc = static_cast<int>(t % atoms_per_block);    // 64-value chunk = scale atom
-    const long long lrb = t / atoms_per_block;                // batch * row_blocks + row block
+    const int kc = static_cast<int>(t % atoms_per_block);  // 64-value chunk = scale atom
+    const long long lrb = t / atoms_per_block;              // batch * row_blocks + row block
     const int rb = static_cast<int>(lrb % row_blocks);
     const int l = static_cast<int>(lrb / row_blocks);
-    uint32_t w[4];
+    const bool kvalid = kc * 4 + b < kblocks;
+#pragma unroll 1
+    for (int g0 = 0; g0 < 32; g0 += kRowGroupsPerBatch) {
+      uint4 v[kRowGroupsPerBatch];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int row = rb * 128 + q * 32 + lane;
-      uint32_t word = 0;
-      if (row < rows) {
-        const long long r = static_cast<long long>(l) * rows + row;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int c = kc * 4 + b;                               // 16-value block along K
-          if (c < kblocks)
-            word |= quantize_block<kF16>(x + r * K + c * 16, codes + r * (K / 2) + c * 8) << (8 * b);
-        }
+      for (int u = 0; u < kRowGroupsPerBatch; ++u) {
+        const int row = rb * 128 + (g0 + u) * 4 + sub;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < rows && kvalid)
+          v[u] = __ldcs(reinterpret_cast<const uint4*>(x + (static_cast<long long>(l) * rows + row) * K +
+                                                       kc * 64 + j * 8));
       }
-      w[q] = word;
+#pragma unroll
+      for (int u = 0; u < kRowGroupsPerBatch; ++u) {
+        const int rin = (g0 + u) * 4 + sub;  // row inside the 128-row block
+        const int row = rb * 128 + rin;
+        float f[8];
+        unpack8<kF16>(v[u], f);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
+        const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+        uint32_t word = 0;
+        if (d != 0.0f) {
+          const float r = __frcp_rn(d);
+          float q[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float q0 = __fmul_rn(f[i], r);
+            q[i] = __fmaf_rn(__fmaf_rn(-q0, d, f[i]), r, q0);
+          }
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            word |= (e2m1x2(q[2 * i], q[2 * i + 1]) | ((w[i] >> 12) & 0x8u) | ((w[i] >> 24) & 0x80u)) << (8 * i);
+        }
+        if (row < rows && kvalid)
+          *reinterpret_cast<uint32_t*>(codes + (static_cast<long long>(l) * rows + row) * (K / 2) + kc * 32 + j * 4) =
+              word;
+        if ((j & 1) == 0) atom[(rin & 31) * 16 + (rin >> 5) * 4 + b] = static_cast<uint8_t>(sc);
+      }
     }
-    *reinterpret_cast<uint4*>(sf + (lrb * atoms_per_block + kc) * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncwarp();
+    *reinterpret_cast<uint4*>(sf + (lrb * atoms_per_block + kc) * 512 + lane * 16) =
+        *reinterpret_cast<const uint4*>(atom + lane * 16);
+    __syncwarp();
   }
 }
 
 }  // namespace
 
-cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, int rows, int K, int L, int sms,
-                            cudaStream_t stream) {
+// Blocks of the quantize kernel resident per SM (0 on error).
+int quantize_blocks_per_sm(int is_f16) {
+  int n = 0;
+  cudaError_t e = is_f16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<true>, kThreads, 0)
+                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel<false>, kThreads, 0);
+  return e == cudaSuccess ? n : 0;
+}
+
+// `max_blocks`: blocks resident at once on the device (one wave).
+cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, int rows, int K, int L,
+                            int max_blocks, cudaStream_t stream) {
   const int row_blocks = (rows + 127) / 128;
   const int atoms_per_block = (K + 255) / 256 * 4;
   const long long tasks = static_cast<long long>(L) * row_blocks * atoms_per_block;
-  long long blocks = (tasks + 7) / 8;  // 8 warps per block
-  const long long cap = static_cast<long long>(sms > 0 ? sms : 1) * 16;
-  if (blocks > cap) blocks = cap;
+  long long blocks = (tasks + kThreads / 32 - 1) / (kThreads / 32);
+  if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* c = static_cast<uint8_t*>(codes);
   uint8_t* s = static_cast<uint8_t*>(sf);
   if (is_f16)
-    quantize_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
-                                                                            atoms_per_block);
+    quantize_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
+                                                                                  atoms_per_block);
   else
-    quantize_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
-                                                                             atoms_per_block);
+    quantize_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
+                                                                                   atoms_per_block);
   return cudaGetLastError();
 }
 

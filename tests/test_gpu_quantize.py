@@ -53,6 +53,11 @@ def test_quantize_special_values():
     x[0, 5, :16] = torch.linspace(-0.01, 0.01, 16)           # subnormal scale
     x[0, 6, :] = torch.randn(64) * 1e3
     x[0, 7, 16:32] = 448 * 6                                 # exactly the largest scale
+    x[0, 0, :16] = torch.linspace(-3, 4, 16)                 # a normal block holding signed zeros and
+    x[0, 0, 3] = -0.0                                        # values far below a quarter of its scale
+    x[0, 0, 5] = 0.0
+    x[0, 0, 7] = -1e-30
+    x[0, 0, 9] = 1e-30
     _check(x.to(torch.bfloat16), rows, K, 1)
 
 
