@@ -310,12 +310,21 @@ int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
 
 // 2-SM pair tiles (256 x 256, tcgen05 cta_group::2) for clustered plans at
 // BN = 256: each CTA keeps half of B in shared memory, so a stage shrinks
-// from 54 to 38 KB and the ring deepens from 4 to 5 stages.  NVFP4_PAIR = 0
-// keeps the multicast clusters instead.
-bool choose_pair(int cluster, int bn) {
+// from 54 to 38 KB and the ring deepens from 4 to 5 stages.  The price is a
+// longer accumulator hand-off between tiles (the even CTA's MMAs wait for both
+// CTAs' epilogues), so pairs are chosen only when tiles average at least
+// kPairMinKtiles k-tiles (GB300: 8192^3, 32 k-tiles: 205 -> 194 us; the
+// two-group workload, 12.4 k-tiles on average: 30.0 us with multicast pairs,
+// 31.2 us with 2-SM pairs).  NVFP4_PAIR = 0 | 1 overrides.
+constexpr int kPairMinKtiles = 16;
+
+bool choose_pair(const Schedule& s, int cluster, int bn) {
   if (cluster != 2 || bn != 256) return false;
   if (const char* env = getenv("NVFP4_PAIR")) return atoi(env) != 0;
-  return true;
+  long long kt = 0;
+  for (int g = 0; g < s.num_groups; ++g)
+    kt += static_cast<long long>(s.tile_start[g + 1] - s.tile_start[g]) * s.ktiles[g];
+  return kt >= static_cast<long long>(kPairMinKtiles) * s.total_tiles;
 }
 
 // Cluster reduction (NVFP4_SKRED = 0 disables): a stream-K plan whose CTAs
@@ -430,7 +439,7 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     const long long per_wave = sms / pl->cluster;
     pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * pl->cluster);
   }
-  pl->pair = !pl->red && choose_pair(pl->cluster, pl->bn);
+  pl->pair = !pl->red && choose_pair(s, pl->cluster, pl->bn);
   pl->stages = gemm_stages(pl->bn, pl->pair);
   return NVFP4_OK;
 }

@@ -268,7 +268,7 @@ def test_parity_pair_tiles_grouped(monkeypatch):
     monkeypatch.setenv("NVFP4_BN", "256")
     monkeypatch.setenv("NVFP4_SCHEDULE", "dp")
     monkeypatch.setenv("NVFP4_CLUSTER", "2")
-    monkeypatch.delenv("NVFP4_PAIR", raising=False)
+    monkeypatch.setenv("NVFP4_PAIR", "1")    # short K: the planner alone would pick multicast pairs
     Ms, Ns, Ks = [256, 512, 200], [512, 264, 1024], [1024, 512, 768]
     plan = binding.nvfp4_gemm_plan(Ms, Ns, Ks, [1] * 3, torch.cuda.get_device_properties(0).multi_processor_count)
     assert plan["pair"] == 1
