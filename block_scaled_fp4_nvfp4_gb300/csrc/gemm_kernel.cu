@@ -1,20 +1,24 @@
 // Persistent, warp-specialised NVFP4 block-scaled GEMM for sm_103a.
 //
 // One CTA per SM walks a static list of work units (output tile, K range) of
-// all groups.  Inside a CTA:
-//   warp 0      TMA producer: per 256-wide k-tile, one 3-D tensor copy each for
-//               the A tile (128 rows x 128 B) and the B tile (BN rows x 128 B)
-//               plus contiguous bulk copies of the scale atoms, all counted on
-//               the stage's "full" mbarrier;
-//   warp 1      MMA issuer (one thread): moves the k-tile's scale atoms into
-//               tensor memory with tcgen05.cp, issues four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64)
-//               into a tensor-memory accumulator and commits the stage back;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one row per thread),
-//               fp32 -> fp16 (RNE), 128B-swizzled staging in shared memory and
-//               TMA tensor stores of 32 x 64 boxes (rows past M are clipped).
-// Split-K units write fp32 partials to a workspace; the last unit of a tile to
-// arrive sums all partials in split order (deterministic) and stores C.
+// all groups.  Inside a CTA (224 threads):
+//   warps 0-1   TMA producers: per 256-wide k-tile warp 0 arms the stage's
+//               "full" mbarrier and copies the A tile (128 rows x 128 B) and
+//               its scale slab, warp 1 the B tile (BN rows x 128 B, or this
+//               CTA's half of it when two CTAs share it) and its scale slabs;
+//   warp 2      MMA issuer (one elected lane): per MMA k-block its scale atoms
+//               into tensor memory with tcgen05.cp, then one
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64,
+//               or 256 x BN x 64 over a CTA pair) into a tensor-memory
+//               accumulator; one commit per k-tile frees the stage;
+//   warps 3-6   epilogue, one per 32-lane tensor-memory sub-partition:
+//               tcgen05.ld of the accumulator (one row per thread), fp32 ->
+//               fp16 (RNE), 64B-swizzled staging and TMA stores of 32 x 32
+//               boxes (rows past M and columns past N are clipped).
+// Stream-K segments of a tile either exchange fp32 partials through
+// distributed shared memory (the tile's segments form one cluster) or write
+// them to a workspace where the last segment to arrive sums them; both sum in
+// segment (k) order, so results are deterministic.
 //
 // The warp roles and the mbarrier ring follow the structure of the pages'
 // kernels ("nvfp4 group gemm, submission 407526", grouped_kernel; "nvfp4 gemm,
