@@ -24,11 +24,12 @@
 // block, q0 = RN(x r) (within one ulp of x / d), and Markstein's correction
 // step (P. Markstein, IBM J. Res. Develop. 34(1), 1990; Handbook of
 // Floating-Point Arithmetic, theorem on division with a correctly rounded
-// reciprocal) q = RN(q0 + RN(x - d q0) r), the remainder exact by FMA, is the
-// correctly rounded quotient when nothing underflows.  Values small enough to
-// underflow there are below a quarter of d and get code 0 whatever the
-// rounding.  The sign bit of each code is taken from the input's own sign bit,
-// so -0.0 keeps it.
+// reciprocal) q = RN(q0 - RN(q0 d - x) r), the residual exact by FMA, is the
+// correctly rounded quotient when nothing underflows (bf16 / fp16 values
+// divided by an E4M3 scale stay far above the fp32 underflow threshold).  The
+// residual is formed as q0 d + (-x) and subtracted, so a signed zero x gives
+// q = x: -0.0 keeps its sign bit.  Both steps run on packed fp32 pairs
+// (fma.rn.f32x2), and block maxima on packed bf16 / fp16 pairs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -49,23 +50,52 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
+// Two packed fp32 values in one 64-bit register, for the f32x2 instructions.
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ uint64_t mul_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Eight 16-bit values (one uint4) -> four packed fp32 pairs, and the same
+// pairs negated; plus the largest magnitude of the eight (exact).
 template <bool kF16>
-__device__ __forceinline__ void unpack8(const uint4 v, float* f) {
+__device__ __forceinline__ float unpack8(const uint4 v, uint64_t* x2, uint64_t* nx2) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float amax = 0.0f;
+  if constexpr (kF16) {
+    __half2 m = __habs2(*reinterpret_cast<const __half2*>(&w[0]));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (kF16) {
-      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-      const float2 t = __half22float2(h);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    } else {
-      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-      const float2 t = __bfloat1622float2(h);
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
+    for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __half2*>(&w[i])));
+    amax = fmaxf(__low2float(m), __high2float(m));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      x2[i] = pack_f2(t.x, t.y);
+      nx2[i] = pack_f2(-t.x, -t.y);
+    }
+  } else {
+    __nv_bfloat162 m = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0]));
+#pragma unroll
+    for (int i = 1; i < 4; ++i) m = __hmax2(m, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[i])));
+    amax = fmaxf(__low2float(m), __high2float(m));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // bf16 -> fp32 is the bit pattern shifted into the upper half
+      const uint64_t lo = static_cast<uint64_t>(w[i] << 16), hi = static_cast<uint64_t>(w[i] & 0xFFFF0000u);
+      x2[i] = lo | (hi << 32);
+      nx2[i] = x2[i] ^ 0x8000000080000000ull;
     }
   }
+  return amax;
 }
 
 constexpr int kRowGroupsPerBatch = 4;  // groups of 4 rows loaded before any is processed
@@ -107,27 +137,22 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
       for (int u = 0; u < kRowGroupsPerBatch; ++u) {
         const int rin = (g0 + u) * 4 + sub;  // row inside the 128-row block
         const int row = rb * 128 + rin;
-        float f[8];
-        unpack8<kF16>(v[u], f);
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        uint64_t x2[4], nx2[4];
+        float amax = unpack8<kF16>(v[u], x2, nx2);
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
         const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
         uint32_t word = 0;
         if (d != 0.0f) {
           const float r = __frcp_rn(d);
-          float q[8];
+          const uint64_t r2 = pack_f2(r, r), nr2 = pack_f2(-r, -r), d2 = pack_f2(d, d);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float q0 = __fmul_rn(f[i], r);
-            q[i] = __fmaf_rn(__fmaf_rn(-q0, d, f[i]), r, q0);
+          for (int i = 0; i < 4; ++i) {
+            const uint64_t q0 = mul_f2(x2[i], r2);
+            const uint64_t q = fma_f2(fma_f2(q0, d2, nx2[i]), nr2, q0);
+            word |= e2m1x2(__uint_as_float(static_cast<uint32_t>(q)), __uint_as_float(static_cast<uint32_t>(q >> 32)))
+                    << (8 * i);
           }
-          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            word |= (e2m1x2(q[2 * i], q[2 * i + 1]) | ((w[i] >> 12) & 0x8u) | ((w[i] >> 24) & 0x80u)) << (8 * i);
         }
         if (row < rows && kvalid)
           *reinterpret_cast<uint32_t*>(codes + (static_cast<long long>(l) * rows + row) * (K / 2) + kc * 32 + j * 4) =
