@@ -29,7 +29,9 @@
 // divided by an E4M3 scale stay far above the fp32 underflow threshold).  The
 // residual is formed as q0 d + (-x) and subtracted, so a signed zero x gives
 // q = x: -0.0 keeps its sign bit.  Both steps run on packed fp32 pairs
-// (fma.rn.f32x2), and block maxima on packed bf16 / fp16 pairs.
+// (fma.rn.f32x2), and block maxima on packed bf16 / fp16 pairs.  The same
+// step with the correctly rounded constant 1/6 gives amax / 6, and a table in
+// shared memory holds d and 1/d for the 128 non-negative E4M3 codes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -107,6 +109,12 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
                                                             int rows, int K, int L, int row_blocks,
                                                             int atoms_per_block) {
   __shared__ __align__(16) uint8_t atoms[kThreads / 32][512];  // one scale atom per warp
+  __shared__ float2 scale_tab[128];                             // {d, 1/d} per E4M3 code 0..127
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+    const float dv = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3)));
+    scale_tab[c] = make_float2(dv, c != 0 ? __frcp_rn(dv) : 0.0f);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   uint8_t* atom = atoms[threadIdx.x >> 5];
   const int sub = lane >> 3;  // row of a group of 4 rows
@@ -140,11 +148,15 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const uint16_t* __re
         uint64_t x2[4], nx2[4];
         float amax = unpack8<kF16>(v[u], x2, nx2);
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(__fdiv_rn(amax, 6.0f), __NV_SATFINITE, __NV_E4M3);
-        const float d = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
+        constexpr float kSixth = 1.0f / 6.0f;  // correctly rounded reciprocal of 6
+        const float a0 = __fmul_rn(amax, kSixth);
+        const float a6 = __fmaf_rn(__fmaf_rn(-a0, 6.0f, amax), kSixth, a0);  // amax / 6, correctly rounded
+        const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(a6, __NV_SATFINITE, __NV_E4M3);
+        const float2 dr = scale_tab[sc & 0x7F];
+        const float d = dr.x;
         uint32_t word = 0;
         if (d != 0.0f) {
-          const float r = __frcp_rn(d);
+          const float r = dr.y;
           const uint64_t r2 = pack_f2(r, r), nr2 = pack_f2(-r, -r), d2 = pack_f2(d, d);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
