@@ -361,6 +361,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     // pair only the even CTA's MMA warp runs; its MMAs, scale copies and
     // commits act on both CTAs.
     constexpr uint32_t idesc = make_idesc_nvf4(P2 ? 2 * kBM : kBM, BN);
+    // Descriptors of stage 0.  Another stage, MMA k-block or scale atom
+    // differs only in the start-address field (bits 0-13, address >> 4; every
+    // address here is below 256 KB, so the field never carries), so the loop
+    // adds constants instead of rebuilding 20 descriptors per k-tile: the
+    // tensor pipe's queue is shallow, and the issue gap between two k-tiles'
+    // MMAs is time the pipe sits idle.
+    const uint64_t dA0 = operand_desc(smem_base);
+    const uint64_t dB0 = operand_desc(smem_base + Cfg::kABytes);
+    const uint64_t dSFA0 = scale_desc(smem_base + Cfg::kABytes + Cfg::kBBytes);
+    const uint64_t dSFB0 = dSFA0 + (kSfSlabBytes >> 4);
+    constexpr uint64_t kStageStep = Cfg::kStageBytes >> 4;
+    constexpr uint64_t kAtomStep = kSfAtomBytes >> 4;
+    constexpr uint64_t kSlabStep = kSfSlabBytes >> 4;
+    constexpr uint64_t kKbStep = 32 >> 4;  // 64 E2M1 codes = 32 bytes per row per MMA
+    static_assert(Cfg::kDynSmem + 2048 < (1 << 18), "shared addresses fit the 14-bit descriptor field");
+    const uint32_t sf_tmem0 = tmem + Cfg::kSfBaseCol;
     int stage = 0;
     uint32_t phase = 0;
     int ab = 0;
@@ -376,6 +392,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       }
       ptx::tc_fence_after_sync();
       const uint32_t d_tmem = tmem + ab * BN;
+      // A 64-wide tile uses the upper half of its 128-row B scale atom when
+      // it starts at row 64 of the atom: column j holds rows 32j..32j+31
+      // ("nvfp4 group gemm, submission 407526": sfb_lane).
+      const uint32_t sfb_col0 = BN < 128 ? static_cast<uint32_t>((x.tn * BN) % 128 / 32) : 0u;
       for (int kt = x.kt0; kt < x.kt1; ++kt) {
         if (!warp_wait(W, full_bar(stage), phase, kStatusTimeoutMma)) {
           ok = false;
@@ -387,16 +407,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // No tcgen05 fence here: the copies and MMAs only read shared memory
         // that the completed phase made visible, and a fence per k-tile
         // would hold back the tensor pipe.
-        const int slot = stage;
-        const uint32_t sA = smem_base + stage * Cfg::kStageBytes;
-        const uint32_t sB = sA + Cfg::kABytes;
-        const uint32_t sSFA = sB + Cfg::kBBytes;
-        const uint32_t sSFB = sSFA + kSfSlabBytes;
-        const uint32_t sfa_t = tmem + Cfg::kSfBaseCol + slot * Cfg::kSfSlotCols;
-        // A 64-wide tile uses the upper half of its 128-row B scale atom when
-        // it starts at row 64 of the atom: column j holds rows 32j..32j+31
-        // ("nvfp4 group gemm, submission 407526": sfb_lane).
-        const uint32_t sfb_col0 = BN < 128 ? static_cast<uint32_t>((x.tn * BN) % 128 / 32) : 0u;
+        const uint64_t so = static_cast<uint64_t>(stage) * kStageStep;
+        const uint64_t dA = dA0 + so, dB = dB0 + so, dSFA = dSFA0 + so, dSFB = dSFB0 + so;
+        const uint32_t sfa_t = sf_tmem0 + stage * Cfg::kSfSlotCols;
         const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
         // Per MMA k-block: its scale atoms -> tensor memory, then the MMA, so
         // the copies of k-block kb+1 can proceed while the MMA of kb runs.
@@ -405,13 +418,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
           if constexpr (P2)
-            ptx::tc_copy_sf2_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+            ptx::tc_copy_sf2_elect(sfa_t + 4 * kb, dSFA + kb * kAtomStep);
           else
-            ptx::tc_copy_sf_elect(sfa_t + 4 * kb, scale_desc(sSFA + kb * kSfAtomBytes));
+            ptx::tc_copy_sf_elect(sfa_t + 4 * kb, dSFA + kb * kAtomStep);
 #pragma unroll
           for (int j = 0; j < Cfg::kSfbBlocks; ++j) {
             const uint32_t t = sfb_t + kb * Cfg::kSfbKbCols + 4 * j;
-            const uint64_t d = scale_desc(sSFB + j * kSfSlabBytes + kb * kSfAtomBytes);
+            const uint64_t d = dSFB + j * kSlabStep + kb * kAtomStep;
             if constexpr (P2)
               ptx::tc_copy_sf2_elect(t, d);
             else
@@ -420,11 +433,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
           const uint32_t acc = (kt > x.kt0 || kb > 0) ? 1u : 0u;
           if constexpr (P2)
-            ptx::tc_mma2_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
-                                    sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols, acc);
+            ptx::tc_mma2_nvf4_elect(d_tmem, dA + kb * kKbStep, dB + kb * kKbStep, idesc, sfa_t + 4 * kb,
+                                    sfb_t + kb * Cfg::kSfbKbCols, acc);
           else
-            ptx::tc_mma_nvf4_elect(d_tmem, operand_desc(sA + kb * 32), operand_desc(sB + kb * 32), idesc,
-                                   sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
+            ptx::tc_mma_nvf4_elect(d_tmem, dA + kb * kKbStep, dB + kb * kKbStep, idesc, sfa_t + 4 * kb,
+                                   sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
         }
         if constexpr (P2)
           ptx::tc_commit2_mc_elect(empty_bar(stage), kPeers);  // the stage is free in both CTAs
