@@ -417,27 +417,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // column j of it holds rows 32j..32j+31.
 #pragma unroll
         for (int kb = 0; kb < kBK / kMmaK; ++kb) {
-          if constexpr (P2)
-            ptx::tc_copy_sf2_elect(sfa_t + 4 * kb, dSFA + kb * kAtomStep);
-          else
-            ptx::tc_copy_sf_elect(sfa_t + 4 * kb, dSFA + kb * kAtomStep);
-#pragma unroll
-          for (int j = 0; j < Cfg::kSfbBlocks; ++j) {
-            const uint32_t t = sfb_t + kb * Cfg::kSfbKbCols + 4 * j;
-            const uint64_t d = dSFB + j * kSlabStep + kb * kAtomStep;
-            if constexpr (P2)
-              ptx::tc_copy_sf2_elect(t, d);
-            else
-              ptx::tc_copy_sf_elect(t, d);
-          }
           // 64 E2M1 codes = 32 bytes per row per MMA: advance inside the swizzle row.
           const uint32_t acc = (kt > x.kt0 || kb > 0) ? 1u : 0u;
-          if constexpr (P2)
-            ptx::tc_mma2_nvf4_elect(d_tmem, dA + kb * kKbStep, dB + kb * kKbStep, idesc, sfa_t + 4 * kb,
-                                    sfb_t + kb * Cfg::kSfbKbCols, acc);
-          else
-            ptx::tc_mma_nvf4_elect(d_tmem, dA + kb * kKbStep, dB + kb * kKbStep, idesc, sfa_t + 4 * kb,
-                                   sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
+          ptx::tc_kblock_elect<P2 ? 2 : 1, Cfg::kSfbBlocks>(
+              sfa_t + 4 * kb, dSFA + kb * kAtomStep, sfb_t + kb * Cfg::kSfbKbCols, dSFB + kb * kAtomStep,
+              sfb_t + kb * Cfg::kSfbKbCols + 4, dSFB + kSlabStep + kb * kAtomStep, d_tmem, dA + kb * kKbStep,
+              dB + kb * kKbStep, idesc, sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
         }
         if constexpr (P2)
           ptx::tc_commit2_mc_elect(empty_bar(stage), kPeers);  // the stage is free in both CTAs

@@ -316,6 +316,46 @@ __device__ __forceinline__ void tc_mma_nvf4_elect(uint32_t d_tmem, uint64_t a_de
 }
 
 
+// One MMA k-block in one instruction group under a single elect.sync: the
+// scale-atom copies into tensor memory (SFA, then NSFB atoms of SFB) and the
+// block-scaled MMA that reads them.  `CG` is the cta_group (1 or 2).
+#define NVFP4_CP(CG, T, D) "@e tcgen05.cp.cta_group::" #CG ".32x128b.warpx4 [%" #T "], %" #D ";\n\t"
+#define NVFP4_MMA(CG) \
+  "@e tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.block16 [%4], %5, %6, %7, [%8], [%9], p;\n\t"
+template <int CG, int NSFB>
+__device__ __forceinline__ void tc_kblock_elect(uint32_t sfa_t, uint64_t sfa_d, uint32_t sfb_t, uint64_t sfb_d,
+                                                uint32_t sfb_t2, uint64_t sfb_d2, uint32_t d_tmem, uint64_t a_desc,
+                                                uint64_t b_desc, uint32_t idesc, uint32_t sfa_mma, uint32_t sfb_mma,
+                                                uint32_t accumulate) {
+  static_assert((CG == 1 || CG == 2) && (NSFB == 1 || NSFB == 2), "variants");
+  if constexpr (CG == 1 && NSFB == 1)
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %10, 0;\n\telect.sync _|e, 0xffffffff;\n\t" NVFP4_CP(1, 0, 1)
+                     NVFP4_CP(1, 2, 3) NVFP4_MMA(1) "}" ::"r"(sfa_t),
+                 "l"(sfa_d), "r"(sfb_t), "l"(sfb_d), "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_mma),
+                 "r"(sfb_mma), "r"(accumulate), "r"(sfb_t2), "l"(sfb_d2)
+                 : "memory");
+  else if constexpr (CG == 1 && NSFB == 2)
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %10, 0;\n\telect.sync _|e, 0xffffffff;\n\t" NVFP4_CP(1, 0, 1)
+                     NVFP4_CP(1, 2, 3) NVFP4_CP(1, 11, 12) NVFP4_MMA(1) "}" ::"r"(sfa_t),
+                 "l"(sfa_d), "r"(sfb_t), "l"(sfb_d), "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_mma),
+                 "r"(sfb_mma), "r"(accumulate), "r"(sfb_t2), "l"(sfb_d2)
+                 : "memory");
+  else if constexpr (CG == 2 && NSFB == 1)
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %10, 0;\n\telect.sync _|e, 0xffffffff;\n\t" NVFP4_CP(2, 0, 1)
+                     NVFP4_CP(2, 2, 3) NVFP4_MMA(2) "}" ::"r"(sfa_t),
+                 "l"(sfa_d), "r"(sfb_t), "l"(sfb_d), "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_mma),
+                 "r"(sfb_mma), "r"(accumulate), "r"(sfb_t2), "l"(sfb_d2)
+                 : "memory");
+  else
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %10, 0;\n\telect.sync _|e, 0xffffffff;\n\t" NVFP4_CP(2, 0, 1)
+                     NVFP4_CP(2, 2, 3) NVFP4_CP(2, 11, 12) NVFP4_MMA(2) "}" ::"r"(sfa_t),
+                 "l"(sfa_d), "r"(sfb_t), "l"(sfb_d), "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_mma),
+                 "r"(sfb_mma), "r"(accumulate), "r"(sfb_t2), "l"(sfb_d2)
+                 : "memory");
+}
+#undef NVFP4_CP
+#undef NVFP4_MMA
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
