@@ -531,13 +531,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       if (x.nseg == 1) {
         // Drain the whole accumulator row into registers as fp16 first and
         // release it, so the next tile's MMAs start while this one is stored.
+        // 128 columns per tensor-memory wait (four loads in flight), so a
+        // 256-wide accumulator is drained in two round trips, not four.
         uint32_t h[BN / 2];
+        constexpr int kDrainCols = BN < 128 ? BN : 128;
 #pragma unroll
-        for (int q = 0; q < BN / 64; ++q) {
-          float v[64];
-          load_chunk(t_row + 64 * q, v);
+        for (int q = 0; q < BN / kDrainCols; ++q) {
+          uint32_t r[kDrainCols];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h[32 * q + i] = pack_half2(v[2 * i], v[2 * i + 1]);
+          for (int c = 0; c < kDrainCols / 32; ++c)
+            ptx::tmem_load_32cols(t_row + kDrainCols * q + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+          ptx::tmem_load_wait();
+#pragma unroll
+          for (int c = 0; c < kDrainCols / 32; ++c) ptx::reg_fence32(&r[32 * c]);
+#pragma unroll
+          for (int i = 0; i < kDrainCols / 2; ++i)
+            h[kDrainCols / 2 * q + i] = pack_half2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         }
         release_acc();
         if (rows_live) {
