@@ -52,7 +52,8 @@ struct SmemCtl {
   uint64_t epi_bcast;
   uint64_t mma_drain;
   uint64_t red_go;    // cluster reduction: every CTA of the cluster may now be written
-  uint64_t red_full;  // cluster reduction: every CTA's slices of this CTA's columns landed
+  uint64_t red_staged;  // cluster reduction: every epilogue warp's staging slots written
+  uint64_t red_full;    // cluster reduction: every peer's slice of this CTA's columns landed
   uint32_t tmem_base;
   volatile int abort;
   int last_flag;
@@ -184,7 +185,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_bcast), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl.mma_drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl.red_go), CL);                 // one arrival per CTA of the cluster
-    ptx::mbar_init(ptx::smem_addr(&ctl.red_full), CL * kEpiWarps * 32);  // every epilogue thread of every CTA
+    ptx::mbar_init(ptx::smem_addr(&ctl.red_staged), kEpiWarps);
+    ptx::mbar_init(ptx::smem_addr(&ctl.red_full), 1);  // armed with the peers' bytes
     ctl.abort = 0;
     ctl.last_flag = 0;
     ptx::fence_mbar_init();
@@ -521,8 +523,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         ptx::tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (P2)
-            ptx::mbar_arrive_cluster(ptx::mapa_shared(acc_empty_bar(my_ab), 0));  // the leader's MMAs wait
+          // A pair's accumulator barrier lives in the even CTA, whose MMAs
+          // overwrite both CTAs' accumulators.  The arrival publishes only
+          // that this warp's tensor-memory reads are complete, so the odd
+          // CTA's remote arrival needs no cluster-scope release.
+          if (P2 && crank != 0)
+            ptx::mbar_arrive_remote(ptx::mapa_shared(acc_empty_bar(my_ab), 0));
           else
             ptx::mbar_arrive(acc_empty_bar(my_ab));
         }
@@ -558,15 +564,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
       if constexpr (kRed) {
         // The CL segments of this tile are the CL CTAs of this cluster (rank
-        // = segment) and each CTA reduces and stores BN/CL of its columns.
-        // Every CTA writes its fp32 partial of those columns into the owner's
-        // shared memory -- the operand ring, idle once a CTA's only work item
-        // is done -- as [BN/CL/4][128 rows][4], and the owner sums the CL
-        // slices in segment (= k) order, as the workspace path does.
+        // = segment) and each CTA reduces and stores BN/CL of the columns.
+        // The operand ring, idle once a CTA's only work item is done, holds
+        // CL receive slots (slot j: segment j's fp32 partial of this CTA's
+        // columns, as [BN/CL/4][128 rows][4]) and then CL staging slots
+        // (staging slot r: this CTA's partial of rank r's columns).  Every
+        // thread drains its row into its own receive slot and the staging
+        // slots; one thread bulk-copies each staging slot into its owner's
+        // receive slot, where the owner's red_full barrier counts the bytes;
+        // the owner sums the CL slots in segment (= k) order, as the
+        // workspace path does.  Each thread reads back only its own row.
         constexpr int kOwnCols = BN / CL;
         constexpr uint32_t kSlotBytes = kOwnCols * kBM * 4;
         static_assert(kOwnCols % 32 == 0, "whole 32-column boxes per CTA");
-        static_assert(CL * kSlotBytes <= kStages * Cfg::kStageBytes, "reduction slices exceed the ring");
+        static_assert(2 * CL * kSlotBytes <= kStages * Cfg::kStageBytes, "reduction slots exceed the ring");
         if (x.nseg != CL || x.seg != crank || red_items++ != 0) {
           if (lane == 0) {
             ctl.abort = 1;
@@ -576,15 +587,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           break;
         }
         const uint32_t go_bar = ptx::smem_addr(&ctl.red_go);
+        const uint32_t staged_bar = ptx::smem_addr(&ctl.red_staged);
         const uint32_t rfull_bar = ptx::smem_addr(&ctl.red_full);
-        // This CTA's MMAs are complete (acc_full), so its ring may be written:
-        // tell every CTA of the cluster, then wait until all of them said so.
-        if (ew == 0 && lane < CL) ptx::mbar_arrive_cluster(ptx::mapa_shared(go_bar, static_cast<uint32_t>(lane)));
-        if (!warp_wait<true>(W, go_bar, 0, kStatusTimeoutEpilogue)) break;
-        uint32_t dst[CL];
+        // This CTA's MMAs are complete (acc_full), so its ring may be
+        // written: tell every CTA of the cluster.
+        if (ew == 0 && lane < CL) ptx::mbar_arrive_remote(ptx::mapa_shared(go_bar, static_cast<uint32_t>(lane)));
+        if (ew == 0 && lane == 0) ptx::mbar_arrive_expect_tx(rfull_bar, (CL - 1) * kSlotBytes);
+        uint32_t slot[CL];
 #pragma unroll
         for (int r = 0; r < CL; ++r)
-          dst[r] = ptx::mapa_shared(smem_base + crank * kSlotBytes + row * 16, static_cast<uint32_t>(r));
+          slot[r] = smem_base + static_cast<uint32_t>(r == static_cast<int>(crank) ? r : CL + r) * kSlotBytes + row * 16;
 #pragma unroll
         for (int q = 0; q < BN / 64; ++q) {
           float v[64];
@@ -592,16 +604,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const int col = 64 * q + 4 * c4;
-            ptx::st_cluster_v4(dst[col / kOwnCols] + (col % kOwnCols) / 4 * (kBM * 16), v[4 * c4], v[4 * c4 + 1],
-                               v[4 * c4 + 2], v[4 * c4 + 3]);
+            st_shared_v4(slot[col / kOwnCols] + (col % kOwnCols) / 4 * (kBM * 16), __float_as_uint(v[4 * c4]),
+                         __float_as_uint(v[4 * c4 + 1]), __float_as_uint(v[4 * c4 + 2]),
+                         __float_as_uint(v[4 * c4 + 3]));
           }
         }
         release_acc();
-        // This thread's slices are written: one arrival at every owner,
-        // releasing the writes at cluster scope.
+        ptx::fence_proxy_async_smem();  // the staging slots are read by bulk copies
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(staged_bar);
+        if (ew == 0) {
+          // every warp's staging written and every CTA of the cluster idle
+          if (!warp_wait(W, staged_bar, 0, kStatusTimeoutEpilogue)) break;
+          if (!warp_wait<true>(W, go_bar, 0, kStatusTimeoutEpilogue)) break;
+          if (lane == 0) {
 #pragma unroll
-        for (int r = 0; r < CL; ++r) ptx::mbar_arrive_cluster(ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
-        if (!warp_wait<true>(W, rfull_bar, 0, kStatusTimeoutEpilogue)) break;
+            for (int r = 0; r < CL; ++r)
+              if (r != static_cast<int>(crank))
+                ptx::bulk_copy_to_cluster(ptx::mapa_shared(smem_base + crank * kSlotBytes, static_cast<uint32_t>(r)),
+                                          smem_base + static_cast<uint32_t>(CL + r) * kSlotBytes, kSlotBytes,
+                                          ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
+          }
+          __syncwarp();
+        }
+        if (!warp_wait(W, rfull_bar, 0, kStatusTimeoutEpilogue)) break;
 #pragma unroll
         for (int cg = 0; cg < kOwnCols / 32; ++cg) {
           float4 acc[8];
@@ -727,10 +753,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   ptx::tc_fence_before_sync();
   __syncthreads();
-  if constexpr (P2) {
+  if constexpr (P2 || kRed) {
     // After an abort a pair CTA may still have copies in flight that only the
-    // leader's barriers count: give them time to land before the shared
-    // memory goes away (they are plain reads of the operands; microseconds).
+    // leader's barriers count, and a cluster-reduction CTA may still be the
+    // source or target of a bulk copy: give them time to land before the
+    // shared memory goes away (plain copies; microseconds).
     if (ctl.abort) {
       if (threadIdx.x == 0) {
         const uint64_t t0 = ptx::globaltimer();

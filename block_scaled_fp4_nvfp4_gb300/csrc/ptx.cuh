@@ -31,8 +31,8 @@ __device__ __forceinline__ void fence_mbar_init() {
 }
 
 // True once the phase with the given parity has completed.
-// try_wait with acquire at cluster scope: pairs with arrivals that release
-// writes made by other CTAs of the cluster (mbar_arrive_cluster).
+// try_wait with acquire at cluster scope, for barriers that other CTAs of
+// the cluster arrive on (mbar_arrive_remote).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -43,14 +43,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
-}
-
-// 16-byte store into the shared memory of a CTA of the cluster
-// (`cluster_addr` from mapa_shared).
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -325,10 +317,30 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address),
-// releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on an mbarrier of any CTA of the cluster (shared::cluster address)
+// with the default CTA-scope release.  For arrivals that publish no ordinary
+// memory writes -- that this CTA's ring is idle, or that this thread's
+// tensor-memory reads are complete (tcgen05.wait::ld) -- a cluster-scope
+// release is not needed, and on GB300 it costs about a microsecond per
+// arrival (it waits for the thread's outstanding memory traffic).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// One thread arms a local barrier with a transaction byte count and arrives.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into the shared memory of a CTA of
+// the cluster; the destination CTA's mbarrier (shared::cluster address)
+// counts the bytes.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
