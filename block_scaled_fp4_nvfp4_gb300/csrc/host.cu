@@ -309,14 +309,13 @@ int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
 }
 
 // 2-SM pair tiles (256 x 256, tcgen05 cta_group::2) for clustered plans at
-// BN = 256: each CTA keeps half of B in shared memory, so a stage shrinks
-// from 54 to 38 KB and the ring deepens from 4 to 5 stages.  The price is a
-// longer accumulator hand-off between tiles (the even CTA's MMAs wait for both
-// CTAs' epilogues), so pairs are chosen only when tiles average at least
-// kPairMinKtiles k-tiles (GB300: 8192^3, 32 k-tiles: 205 -> 194 us; the
-// two-group workload, 12.4 k-tiles on average: 30.0 us with multicast pairs,
-// 31.2 us with 2-SM pairs).  NVFP4_PAIR = 0 | 1 overrides.
-constexpr int kPairMinKtiles = 16;
+// BN = 256: each CTA keeps half of B in shared memory, so a stage -- and what
+// each SM takes in per k-tile -- shrinks from 54 to 38 KB and the ring
+// deepens from 4 to 5 stages.  Chosen when tiles average at least
+// kPairMinKtiles k-tiles; shorter tiles are mostly ring fill (GB300: 8192^3
+// 155 us as pairs; the two-group workload, 12.4 k-tiles per tile on average,
+// 26.3 us as pairs vs 29.7 us with B multicast).  NVFP4_PAIR = 0 | 1 overrides.
+constexpr int kPairMinKtiles = 4;
 
 bool choose_pair(const Schedule& s, int cluster, int bn) {
   if (cluster != 2 || bn != 256) return false;

@@ -270,10 +270,13 @@ def test_pair_tiles_planned_for_wide_clusters(lib, monkeypatch):
     assert p["cluster"] == 2 and p["pair"] == 0
     monkeypatch.delenv("NVFP4_BN")
     assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["pair"] == 0
-    # tiles averaging fewer than 16 k-tiles keep multicast pairs (shorter hand-off between tiles)
+    # the two-group workload (12.4 k-tiles per tile on average) runs as pairs too
     p = binding.nvfp4_gemm_plan([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], 152)
-    assert p["cluster"] == 2 and p["pair"] == 0
+    assert p["cluster"] == 2 and p["pair"] == 1
     assert binding.nvfp4_gemm_plan([2048], [8192], [4096], [1], 152)["pair"] == 1
+    # tiles shorter than one ring (K = 512: 2 k-tiles) keep B multicast
+    p = binding.nvfp4_gemm_plan([4096], [8192], [512], [1], 152)
+    assert p["cluster"] == 2 and p["pair"] == 0
 
 
 def test_cluster_reduction_planned_for_one_segment_per_cta(lib, monkeypatch):
