@@ -187,6 +187,32 @@ def job_throughput(flops_per_step, steps, elapsed_ms_max, world):
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+def size_matched_copy(nbytes, dev, stream, l2, iters=200):
+    """HBM rate of the copy that defines the measured peak (torch copy_,
+    read + write bytes) at the size of one launch: a buffer of nbytes/2
+    copied per launch, rotating over sets that together exceed L2.  A single
+    launch of tens of MB spends a visible part of its time ramping up and
+    draining, so this is the practical ceiling for a launch of that size."""
+    half = max(16, (nbytes // 2) // 16 * 16)
+    nsets = max(2, math.ceil(3 * l2 / (2 * half)) + 1)
+    src = [torch.full((half,), 1, dtype=torch.uint8, device=dev) for _ in range(nsets)]
+    dst = [torch.empty((half,), dtype=torch.uint8, device=dev) for _ in range(nsets)]
+    with torch.cuda.stream(stream):
+        for i in range(nsets):
+            dst[i].copy_(src[i])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(iters):
+            dst[i % nsets].copy_(src[i % nsets])
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / iters * 1e3
+    del src, dst
+    return {"bytes_per_launch": 2 * half, "us": us, "achieved": 2 * half / (us * 1e-6) / 1e9, "unit": "GB/s",
+            "how": "torch copy_ of %.1f MB (read + write), %d buffer pairs rotating, CUDA events" % (
+                half / 1e6, nsets)}
+
+
 def _oracle_columns(p, ncols, threads):
     import oracle
     t0 = time.perf_counter()
@@ -492,6 +518,8 @@ def main():
     else:
         achieved, peak, unit = flops / launch_s / 1e12, fp4_peak, "TFLOP/s"
 
+    copy_ref = size_matched_copy(wl.bytes, dev, stream, l2) if bound == "hbm" else None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v, dt, threads, desc = time_oracle(args.workload, args.cpu_seconds)
@@ -512,7 +540,9 @@ def main():
                          "peak_source": "%s (%s)" % (peak_src, "hbm_gbs" if bound == "hbm" else
                                                      "bf16_tflops x 6 nominal fp4/bf16"),
                          "algorithmic_bytes_per_launch": wl.bytes, "flops_per_launch": flops,
-                         "avg_launch_us": launch_ms * 1e3},
+                         "avg_launch_us": launch_ms * 1e3,
+                         "size_matched_copy": copy_ref,
+                         "frac_of_size_matched_copy": None if copy_ref is None else achieved / copy_ref["achieved"]},
             "roofline_fraction_min_time": max(t_hbm, t_fp4) / launch_s,
             "cpu_baseline": cpu,
             "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
