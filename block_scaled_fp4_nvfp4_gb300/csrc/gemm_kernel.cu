@@ -218,10 +218,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   const uint32_t tmem = ctl.tmem_base;
 
   // Programmatic dependent launch: everything above overlaps the previous
-  // kernel on the stream.  Before waiting for it, one thread asks L2 for the
-  // first k-tiles this CTA will load (operand tiles and scale slabs), so HBM
-  // stays busy while the previous kernel drains; every actual load and store
-  // comes after the wait.
+  // kernel on the stream.  Optionally (prefetch_ktiles > 0) one thread asks L2
+  // for the first k-tiles this CTA will load before waiting for it; every
+  // actual load and store comes after the wait.
   if (warp == 0 && lane == 0 && p.prefetch_ktiles > 0) {
     WorkCursor pc;
     work_begin(p.sched, unit, units, pc, wrank);

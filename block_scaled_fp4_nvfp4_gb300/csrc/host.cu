@@ -244,13 +244,17 @@ struct Plan {
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 // k-tiles each CTA prefetches into L2 before waiting for the preceding kernel
-// (NVFP4_PREFETCH overrides; 0 disables).
+// (NVFP4_PREFETCH = 1..64 enables).  Off by default: back to back on GB300 the
+// prefetches compete with the preceding launch's HBM stream (128 x 7168 x
+// 16384: 17.2 us without, 17.4 / 17.5 / 17.6 / 18.8 / 21.8 us with 1 / 3 / 6 /
+// 16 / 32 k-tiles; the two-group workload 25.8 vs 26.4 us with 6; no change on
+// the others).
 int prefetch_ktiles() {
   if (const char* env = getenv("NVFP4_PREFETCH")) {
     const int v = atoi(env);
     if (v >= 0 && v <= 64) return v;
   }
-  return 6;
+  return 0;
 }
 
 enum SchedMode { kSchedAuto = 0, kSchedDataParallel = 1, kSchedStreamK = 2 };

@@ -438,3 +438,28 @@ def test_cluster_reduction_timeout_is_reported(monkeypatch):
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, 1)
+
+
+_PAIR_ENV = {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2", "NVFP4_PAIR": "1"}
+
+
+@pytest.mark.parametrize("M,N,K,env,variant", [(128, 1024, 4096, {}, "cluster_reduce"),
+                                               (512, 2048, 2048, {}, "cluster_reduce"),
+                                               (384, 4096, 1024, {}, "single"),
+                                               (512, 512, 1024, _PAIR_ENV, "pair")])
+def test_optional_l2_prefetch_changes_no_result(M, N, K, env, variant, monkeypatch):
+    """The optional L2 prefetch of each CTA's first k-tiles before the launch
+    dependency (NVFP4_PREFETCH, off by default) leaves every result as it is,
+    for cluster-reduced stream-K, plain stream-K and 2-SM pair plans alike."""
+    binding = require_gpu()
+    monkeypatch.setenv("NVFP4_PREFETCH", "6")
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    p = workloads.make_random_problem(M + 3 * N + K, M, N, K, 1)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, 1)
+    run_single(d, C)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == variant
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, 1)
