@@ -466,15 +466,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     uint32_t aphase = 0;
     uint32_t gphase = 0;
     [[maybe_unused]] int red_items = 0;
-    // Convert 64 fp32 columns of this thread's row to fp16, stage them as one
-    // 128-byte swizzled row of a 32 x 64 box and let lane 0 store the box.
     // Store 32 columns of this warp's 32 rows, packed as 16 half2 words per
     // thread: 64-byte-swizzled staging (16-byte chunk j of row r at chunk
     // j ^ ((r >> 1) & 3), conflict-free) and one TMA store of the 32 x 32 box.
-    auto store_box = [&](const Work& x, int col, const uint32_t* h) {
-      const uint32_t sbuf = epi_base + ew * Cfg::kEpiBufBytes;
-      if (lane == 0) ptx::bulk_wait_read<0>();  // the previous store has read the buffer
-      __syncwarp();
+    auto stage_and_store = [&](const Work& x, int col, const uint32_t* h, uint32_t sbuf) {
       const uint32_t row_addr = sbuf + lane * 64;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -485,6 +480,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         ptx::tma_store_3d(&p.tmC[x.g], sbuf, x.tn * BN + col, x.tm * kBM + sub * 32, x.l);
         ptx::bulk_commit();
       }
+    };
+    // Through this warp's staging buffer: the store that last read it must
+    // have read it before it is rewritten.
+    auto store_box = [&](const Work& x, int col, const uint32_t* h) {
+      const uint32_t sbuf = epi_base + ew * Cfg::kEpiBufBytes;
+      if (lane == 0) ptx::bulk_wait_read<0>();
+      __syncwarp();
+      stage_and_store(x, col, h, sbuf);
     };
     auto store_chunk = [&](const Work& x, int q, const float* v) {
       uint32_t h[32];
@@ -576,7 +579,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         constexpr int kOwnCols = BN / CL;
         constexpr uint32_t kSlotBytes = kOwnCols * kBM * 4;
         static_assert(kOwnCols % 32 == 0, "whole 32-column boxes per CTA");
-        static_assert(2 * CL * kSlotBytes <= kStages * Cfg::kStageBytes, "reduction slots exceed the ring");
+        static_assert(2 * CL * kSlotBytes + kEpiWarps * (kOwnCols / 32) * Cfg::kEpiBufBytes <= kStages * Cfg::kStageBytes,
+                      "reduction slots and C staging exceed the ring");
         if (x.nseg != CL || x.seg != crank || red_items++ != 0) {
           if (lane == 0) {
             ctl.abort = 1;
@@ -648,7 +652,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
             hs[2 * c4] = pack_half2(acc[c4].x, acc[c4].y);
             hs[2 * c4 + 1] = pack_half2(acc[c4].z, acc[c4].w);
           }
-          if (rows_live) store_box(x, crank * kOwnCols + 32 * cg, hs);
+          // every box its own staging buffer in the idle ring, past the slots
+          if (rows_live)
+            stage_and_store(x, crank * kOwnCols + 32 * cg, hs,
+                            smem_base + 2 * CL * kSlotBytes + (ew * (kOwnCols / 32) + cg) * Cfg::kEpiBufBytes);
         }
         continue;
       }
