@@ -463,3 +463,65 @@ def test_optional_l2_prefetch_changes_no_result(M, N, K, env, variant, monkeypat
     binding.nvfp4_gemm_check_device_status()
     assert_close_full(C, p)
     check_canary(buf, M, N, 1)
+
+
+# Planner overrides crossed with random shapes: every combination either runs
+# as asked or the planner falls back to a valid plan; the results must match
+# the oracle either way.
+_SWEEP_ENVS = [
+    {},
+    {"NVFP4_BN": "64"},
+    {"NVFP4_BN": "128", "NVFP4_SCHEDULE": "dp"},
+    {"NVFP4_BN": "128", "NVFP4_SCHEDULE": "sk"},
+    {"NVFP4_BN": "128", "NVFP4_SCHEDULE": "sk", "NVFP4_SKRED": "0"},
+    {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "1"},
+    {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2", "NVFP4_PAIR": "0"},
+    {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2", "NVFP4_PAIR": "1"},
+    {"NVFP4_BN": "128", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2"},
+    {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "sk"},
+]
+_SWEEP_KEYS = ("NVFP4_BN", "NVFP4_SCHEDULE", "NVFP4_CLUSTER", "NVFP4_PAIR", "NVFP4_SKRED")
+
+
+def _sweep_shapes(case):
+    """1-3 problems; N a multiple of 8 up to 520, K a multiple of 64, L 1-2.
+    Cluster overrides get an even number of 128-row m-tiles (ragged inside
+    the last one); stream-K ones get long K (up to 4096) and few tiles, so
+    that 2- and 4-segment reductions occur."""
+    env = _SWEEP_ENVS[case % len(_SWEEP_ENVS)]
+    rng = np.random.default_rng(1000 + case)
+    wants_cluster = env.get("NVFP4_CLUSTER") == "2"
+    wants_sk = env.get("NVFP4_SCHEDULE") == "sk" or not env
+    shapes = []
+    for _ in range(int(rng.integers(1, 4))):
+        if wants_cluster:
+            M = 256 * int(rng.integers(1, 3)) - int(rng.integers(0, 128))
+        elif wants_sk:
+            M = int(rng.integers(1, 257))
+        else:
+            M = int(rng.choice([int(rng.integers(1, 385)), 128 * int(rng.integers(1, 4))]))
+        N = 8 * int(rng.integers(1, 66))
+        K = 64 * int(rng.integers(16, 65)) if wants_sk else 64 * int(rng.integers(1, 17))
+        L = int(rng.integers(1, 3))
+        shapes.append((M, N, K, L))
+    return shapes
+
+
+@pytest.mark.parametrize("case", range(20))
+def test_random_shapes_and_plans(case, monkeypatch):
+    """Seeded random groups under a rotating planner override (tile width,
+    schedule, clusters, 2-SM pairs, cluster reduction), element by element
+    against the oracle."""
+    binding = require_gpu()
+    shapes = _sweep_shapes(case)
+    for k in _SWEEP_KEYS:
+        monkeypatch.delenv(k, raising=False)
+    for k, v in _SWEEP_ENVS[case % len(_SWEEP_ENVS)].items():
+        monkeypatch.setenv(k, v)
+    probs = [workloads.make_random_problem(5000 + 10 * case + i, *s) for i, s in enumerate(shapes)]
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    _grouped(binding, devs, probs, Cs)
+    for p, (buf, c) in zip(probs, Cs):
+        check_canary(buf, p["M"], p["N"], p["L"])
+        assert_close_full(c, p)
