@@ -321,6 +321,20 @@ int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
 // 26.3 us as pairs vs 29.7 us with B multicast).  NVFP4_PAIR = 0 | 1 overrides.
 constexpr int kPairMinKtiles = 4;
 
+// Padded 2-SM pairs for groups with odd m-tile counts: 0 off, 1 by the rule
+// below, 2 whenever valid (NVFP4_PAD_PAIRS overrides; 2 is for tests).  Off
+// by default: on the eight-group MoE workload (27 m-tiles padded to 30, 240
+// pair tiles for 76 pairs) it measured 47.0 vs 45.4 us, the fourth round of
+// tiles on some pairs outweighing the smaller per-SM intake.
+constexpr int kPadPairsMaxPct = 115;
+int pad_pairs_mode() {
+  if (const char* env = getenv("NVFP4_PAD_PAIRS")) {
+    const int v = atoi(env);
+    if (v >= 0 && v <= 2) return v;
+  }
+  return 0;
+}
+
 bool choose_pair(const Schedule& s, int cluster, int bn) {
   if (cluster != 2 || bn != 256) return false;
   if (const char* env = getenv("NVFP4_PAIR")) return atoi(env) != 0;
@@ -443,6 +457,39 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * pl->cluster);
   }
   pl->pair = !pl->red && choose_pair(s, pl->cluster, pl->bn);
+  if (!pl->red && pl->cluster == 1 && allow_cluster && pl->bn == 256 && s.dp_tiles == s.total_tiles &&
+      pad_pairs_mode() != 0) {
+    // Groups with an odd number of 128-row m-tiles keep clusters from
+    // forming.  2-SM pairs can still run them with one padding m-tile per
+    // such group: A and its scales are read through tensor maps, so the
+    // padding rows load as zeros, and the epilogue stores no row past M.
+    // (B-multicast pairs load the A scales with plain bulk copies and
+    // cannot be padded.)  Taken when the padding adds at most
+    // kPadPairsMaxPct percent of tiles and the pairs fill two waves.
+    long long padded = 0;
+    for (int g = 0; g < G; ++g) padded += static_cast<long long>((pl->tiles_m[g] + 1) & ~1) * pl->tiles_n[g] * L[g];
+    Schedule ps = s;
+    long long t = 0;
+    for (int g = 0; g < G; ++g) {
+      ps.tiles_m[g] = (pl->tiles_m[g] + 1) & ~1;
+      ps.tile_start[g] = static_cast<int>(t);
+      t += static_cast<long long>(ps.tiles_m[g]) * ps.tiles_n[g] * L[g];
+    }
+    ps.tile_start[G] = static_cast<int>(t);
+    ps.total_tiles = ps.dp_tiles = static_cast<int>(t);
+    for (int g = 0; g < G; ++g) ps.sk_tile_first[g] = ps.total_tiles;
+    ps.cluster = 2;
+    const bool worth = pad_pairs_mode() == 2 || (padded * 100 <= tiles * kPadPairsMaxPct && padded >= 2 * sms);
+    if (padded > tiles && worth && choose_pair(ps, 2, pl->bn)) {
+      s = ps;
+      for (int g = 0; g < G; ++g) pl->tiles_m[g] = ps.tiles_m[g];
+      pl->cluster = 2;
+      pl->pair = true;
+      const long long groups = padded / 2;
+      const long long per_wave = sms / 2;
+      pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * 2);
+    }
+  }
   pl->stages = gemm_stages(pl->bn, pl->pair);
   return NVFP4_OK;
 }

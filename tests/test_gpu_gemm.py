@@ -525,3 +525,31 @@ def test_random_shapes_and_plans(case, monkeypatch):
     for p, (buf, c) in zip(probs, Cs):
         check_canary(buf, p["M"], p["N"], p["L"])
         assert_close_full(c, p)
+
+
+@pytest.mark.parametrize("shapes", [[(384, 2048, 1024, 1), (64, 1024, 1024, 1)],
+                                    [(200, 1536, 1024, 1), (100, 512, 1280, 2)],
+                                    [(300, 768, 2048, 2)]])
+def test_padded_pair_tiles(shapes, monkeypatch):
+    """2-SM pairs over groups with an odd number of 128-row m-tiles, each such
+    group padded by one m-tile: the padding rows load as zeros (including the
+    next batch's scale block read past the last row block when L > 1) and are
+    never stored; every real element matches the oracle."""
+    binding = require_gpu()
+    for k, v in {"NVFP4_PAD_PAIRS": "2", "NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp"}.items():
+        monkeypatch.setenv(k, v)
+    for k in ("NVFP4_PAIR", "NVFP4_CLUSTER"):
+        monkeypatch.delenv(k, raising=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K, L = ([s[i] for s in shapes] for i in range(4))
+    plan = binding.nvfp4_gemm_plan(M, N, K, L, sms)
+    padded = sum(((m + 127) // 128 + 1) // 2 * 2 * ((n + 255) // 256) * l for m, n, _, l in shapes)
+    assert plan["pair"] == 1 and plan["tiles"] == padded, plan
+    probs = [workloads.make_random_problem(7000 + 13 * i + m, *s) for i, (m, s) in enumerate(zip(M, shapes))]
+    devs = [to_device(p) for p in probs]
+    Cs = [alloc_c(p["M"], p["N"], p["L"]) for p in probs]
+    _grouped(binding, devs, probs, Cs)
+    assert binding.nvfp4_gemm_last_launch()["variant"] == "pair"
+    for p, (buf, c) in zip(probs, Cs):
+        check_canary(buf, p["M"], p["N"], p["L"])
+        assert_close_full(c, p)
