@@ -4,24 +4,31 @@
 One step = one pass of the hot path over one batch of synthetic input:
 ``nvfp4_gemm_run_grouped`` on inputs already resident in HBM with scales already
 repacked (the repack is a once-per-weight preparation, timed separately in
-``step_with_repack``).  Default workload: the skinny-M problem
-M=128 N=7168 K=16384 (HBM-bound on B).
+``step_with_repack``).
 
-Timing: W untimed warm-up steps, then exactly K steps between a barrier and a
-device synchronisation on both sides, timed with CUDA events on the launching
-stream; the step cycles through R independent input sets whose total size is
-more than three times the L2 cache, so no step finds its operands in L2.
-``e2e`` is the same metric through the C ABI with host buffers: every step
-copies the step's inputs from pinned host memory, repacks both scale tensors,
-runs the GEMM and copies C back, all inside the timed region (two device buffer
-sets, so one step's host-to-device copies overlap the previous step's work).
+Every workload of the problem statement is timed in one run (``per_config``):
+the 128x128x256 single tile, the skinny-M 128x7168x16384 problem, the dense
+8192^3 problem, the two-group and the eight-group MoE problems.  The headline
+``value``, ``roofline``, ``e2e`` and ``cpu_baseline`` belong to the largest
+one, the compute-bound 8192^3 problem (``--workload`` picks another).
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA graphs
+right after one untimed warm replay, timed with CUDA events on the launching
+stream with a device synchronisation on both sides; the steps cycle through R
+independent input sets whose total size is more than three times the L2 cache,
+so no step finds its operands in L2.  ``e2e`` is the same metric through the C
+ABI with host buffers: every step copies the step's inputs from pinned host
+memory, repacks both scale tensors, runs the GEMM and copies C back, all inside
+the timed region (two device buffer sets, so one step's host-to-device copies
+overlap the previous step's work).
 
 ``--impl reference`` times the CPU oracle (the only reference this method has)
 on a bounded sample of the same workload.
 
-Multi-GPU: launched under torchrun, every rank runs the same workload on its own
-GPU (weak scaling; the problems are independent, there is no exchange), the
-time is the max over ranks and ``value`` counts the work of all ranks.
+One GPU only: the library's kernels load shared tiles with cluster multicast,
+which stays within one GPU's memory, and nothing here shards.  Launched with
+more than one rank or ``--gpus`` > 1, rank 0 prints an ``unavailable`` line and
+every rank exits without touching a GPU.
 """
 import argparse
 import hashlib
@@ -41,25 +48,28 @@ import torch  # noqa: E402
 from block_scaled_fp4_nvfp4_gb300 import workloads  # noqa: E402
 
 METRIC = "NVFP4 (grouped) GEMM TFLOPS, device-timed, and % of FP4-tensor/HBM roofline"
-DEFAULT_WORKLOAD = "skinny_128x7168x16384"
+HEADLINE_WORKLOAD = "dense_8192x8192x8192"
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio, used to scale the measured bf16 peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["gemm_kernel.cu", "gemm_params.h", "ptx.cuh", "descriptors.h", "schedule.h"]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--workload", default=HEADLINE_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--configs", default="all",
+                    help="comma-separated workloads timed in per_config ('all', or 'none')")
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--check", action="store_true", help="oracle check of set 0 (sampled)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the fused quantize + repack leg")
-    return ap.parse_args()
+    ap.add_argument("--no-repack-step", action="store_true", help="skip the step_with_repack leg")
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ helpers
@@ -91,15 +101,28 @@ def ncu_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
+def roofline_terms(wl, peaks):
+    """(bound, t_hbm, t_fp4, hbm GB/s, fp4 TFLOP/s) of a workload."""
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fp4 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP4_OVER_BF16
+    t_hbm = wl.bytes / (hbm * 1e9)
+    t_fp4 = wl.flops / (fp4 * 1e12)
+    return ("hbm" if t_hbm >= t_fp4 else "tensor"), t_hbm, t_fp4, hbm, fp4
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons at 100 ms, for the timed region."""
+    """nvidia-smi clocks / throttle reasons every 100 ms, started before the
+    timed regions; each region takes the samples that fall inside it, else the
+    nearest ones (a region shorter than the sampling period)."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.rows = []
         self.path = os.path.join("/tmp", "nvfp4_clocks_%d_%d.csv" % (os.getpid(), index))
 
     def start(self):
@@ -112,16 +135,16 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self, t0, t1):
+    def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
+        time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 10:
@@ -129,64 +152,119 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
+                self.rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
             except (ValueError, IndexError):
                 continue
         os.unlink(self.path)
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+
+    def window(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [r for r in self.rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
         window = "timed"
         if not inside:
-            # timed region shorter than the sampling period: nearest samples
-            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
-            window = "adjacent (timed region %.3f s, shorter than the 0.1 s sampling period)" % (t1 - t0)
+            inside = sorted(self.rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+            window = "adjacent (timed region %.4f s, shorter than the 0.1 s sampling period)" % (t1 - t0)
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for r in inside:
-            flags = r[4][1:5]
-            for n, fl in zip(names, flags):
+            for n, fl in zip(self.NAMES, r[4][1:5]):
                 if fl.lower().startswith("active"):
                     reasons.add(n)
+
+        def watts(s):
+            try:
+                return float(s)
+            except ValueError:
+                return 0.0
         return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
-                "power_w_max": max(float(r[3]) if r[3].replace(".", "", 1).isdigit() else 0.0 for r in inside),
-                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+                "power_w_max": max(watts(r[3]) for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "window": window}
 
 
-def dist_setup():
+def one_gpu_only(args):
+    """True (after printing the line on rank 0) when asked for more than one GPU."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x, world, device="cuda"):
-    """Largest value over all ranks (the job takes as long as its slowest rank)."""
-    if world <= 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def job_throughput(flops_per_step, steps, elapsed_ms_max, world):
-    """Whole-job TFLOP/s under weak scaling: every rank ran `steps` steps of
-    the same workload; the job took the slowest rank's time."""
-    return flops_per_step * steps * world / (elapsed_ms_max * 1e-3) / 1e12
+    if args.gpus <= 1 and world <= 1:
+        return False
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps({"impl": args.impl, "metric": METRIC, "n_gpus": max(args.gpus, world),
+                          "unavailable": "one GPU only: the GEMM runs on a single GB300 and nothing "
+                                         "shards; no multi-GPU path is built"}), flush=True)
+    return True
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+def _oracle_columns(p, ncols, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gemm(p["A"], p["B"][:, :ncols].contiguous(), p["SFA"], p["SFB"][:, :ncols].contiguous(),
+                p["M"], ncols, p["K"], 1, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def _oracle_sample(wl, seed=0):
+    import oracle
+    probs = workloads.make_inputs(wl, seed=seed)
+    p = max(probs, key=lambda q: q["M"] * q["N"] * q["K"])
+    p = dict(p, A=p["A"][:1], B=p["B"][:1], SFA=p["SFA"][:1], SFB=p["SFB"][:1])
+    return p, oracle.max_threads()
+
+
+def time_oracle(wl, target_s, seed=0):
+    """Time the oracle (as it stands) on whole output columns of the workload's
+    largest group, growing the sample until it takes about target_s.  Returns
+    (TFLOP/s, seconds, threads, description)."""
+    p, threads = _oracle_sample(wl, seed)
+    M, N, K = p["M"], p["N"], p["K"]
+    ncols = 1
+    while True:
+        dt = _oracle_columns(p, ncols, threads)
+        if dt >= target_s * 0.5 or ncols >= N:
+            break
+        ncols = min(N, max(ncols * 2, int(ncols * target_s / max(dt, 1e-3) * 0.9)))
+    desc = "oracle on %d of %d output columns of the %dx%dx%d problem (all %d rows), %d threads" % (
+        ncols, N, M, N, K, M, threads)
+    return 2.0 * M * ncols * K / dt / 1e12, dt, threads, desc
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores, each step a
+    bounded sample (whole output columns) sized so the run ends in minutes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    wl = workloads.WORKLOADS[args.workload]
+    p, threads = _oracle_sample(args.workload)
+    M, N, K = p["M"], p["N"], p["K"]
+    t1 = _oracle_columns(p, 1, threads)
+    t2 = _oracle_columns(p, 2, threads)
+    per_col = max(t2 - t1, t1 / 2, 1e-6)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    ncols = int(max(1, min(N, budget / per_col)))
+    secs = []
+    for i in range(args.warmup + args.steps):
+        dt = _oracle_columns(p, ncols, threads)
+        if i >= args.warmup:
+            secs.append(dt)
+    step_s = float(np.mean(secs)) if secs else float("nan")
+    value = 2.0 * M * ncols * K / step_s / 1e12
+    desc = "oracle on %d of %d output columns of the %dx%dx%d problem (all %d rows) per step, %d threads" % (
+        ncols, N, M, N, K, M, threads)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "shapes_MNKL": wl.shapes, "seed": 0},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU timing
 def size_matched_copy(nbytes, dev, stream, l2, iters=200):
     """HBM rate of the copy that defines the measured peak (torch copy_,
     read + write bytes) at the size of one launch: a buffer of nbytes/2
@@ -213,99 +291,14 @@ def size_matched_copy(nbytes, dev, stream, l2, iters=200):
                 half / 1e6, nsets)}
 
 
-def _oracle_columns(p, ncols, threads):
-    import oracle
-    t0 = time.perf_counter()
-    oracle.gemm(p["A"], p["B"][:, :ncols].contiguous(), p["SFA"], p["SFB"][:, :ncols].contiguous(),
-                p["M"], ncols, p["K"], 1, nthreads=threads)
-    return time.perf_counter() - t0
-
-
-def _oracle_sample(wl, seed=0):
-    import oracle
-    probs = workloads.make_inputs(wl, seed=seed)
-    p = max(probs, key=lambda q: q["N"] * q["K"])
-    p = dict(p, A=p["A"][:1], B=p["B"][:1], SFA=p["SFA"][:1], SFB=p["SFB"][:1])
-    return p, oracle.max_threads()
-
-
-def time_oracle(wl, target_s, seed=0):
-    """Time the oracle (as it stands) on whole output columns of the workload's
-    largest group, growing the sample until it takes about target_s.  Returns
-    (TFLOP/s, seconds, threads, description)."""
-    p, threads = _oracle_sample(wl, seed)
-    M, N, K = p["M"], p["N"], p["K"]
-    ncols = 8
-    while True:
-        dt = _oracle_columns(p, ncols, threads)
-        if dt >= target_s * 0.5 or ncols >= N:
-            break
-        ncols = min(N, max(ncols * 2, int(ncols * target_s / max(dt, 1e-3) * 0.9)))
-    desc = "oracle on %d of %d output columns of the %dx%dx%d problem (all %d rows), %d threads" % (
-        ncols, N, M, N, K, M, threads)
-    return 2.0 * M * ncols * K / dt / 1e12, dt, threads, desc
-
-
-def run_reference(args):
-    """The reference arm: the CPU oracle timed on the host cores, each step a
-    bounded sample (whole output columns) sized so the run ends in minutes."""
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
-        return
-    wl = workloads.WORKLOADS[args.workload]
-    p, threads = _oracle_sample(args.workload)
-    M, N, K = p["M"], p["N"], p["K"]
-    t1 = _oracle_columns(p, 1, threads)
-    t8 = _oracle_columns(p, 8, threads)
-    per_col = max((t8 - t1) / 7.0, 1e-6)
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    ncols = int(max(1, min(N, (budget - t1) / per_col + 1)))
-    secs = []
-    for i in range(args.warmup + args.steps):
-        dt = _oracle_columns(p, ncols, threads)
-        if i >= args.warmup:
-            secs.append(dt)
-    step_s = float(np.mean(secs)) if secs else float("nan")
-    value = 2.0 * M * ncols * K / step_s / 1e12
-    desc = "oracle on %d of %d output columns of the %dx%dx%d problem (all %d rows) per step, %d threads" % (
-        ncols, N, M, N, K, M, threads)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "shapes_MNKL": wl.shapes, "seed": 0},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-
-
-# ------------------------------------------------------------------ our arm
-def main():
-    args = parse()
-    if args.impl == "reference":
-        return run_reference(args)
-    world, rank, local = dist_setup()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from block_scaled_fp4_nvfp4_gb300 import binding
-    binding.load_library()
-
-    wl = workloads.WORKLOADS[args.workload]
-    G = len(wl.shapes)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
-    sets = max(2, math.ceil(3 * l2 / wl.bytes) + 1)
-
-    # ---- inputs: R independent seeded sets, resident in HBM, scales repacked
-    host_sets = []
+def device_inputs(binding, wl, sets, dev):
+    """R seeded input sets of a workload on the device, scales repacked."""
+    host0 = None
     dev_sets = []
     for r in range(sets):
         probs = workloads.make_inputs(wl, seed=r)
         if r == 0:
-            host_sets.append(probs)
+            host0 = probs
         d = []
         for p in probs:
             M, N, K, L = p["M"], p["N"], p["K"], p["L"]
@@ -318,39 +311,44 @@ def main():
             d.append(q)
         dev_sets.append(d)
     torch.cuda.synchronize()
+    return host0, dev_sets
 
-    def launch(d, stream=None):
-        binding.nvfp4_gemm_run_grouped(
-            G, [q["A"] for q in d], [q["B"] for q in d], [q["SFA"] for q in d], [q["SFB"] for q in d],
-            [q["C"] for q in d], [q["M"] for q in d], [q["N"] for q in d], [q["K"] for q in d],
-            [q["L"] for q in d], stream)
 
-    # All launches go to one dedicated stream: the warm-up sizes the library's
-    # per-stream split-K workspace before the timed steps are captured.
-    stream = torch.cuda.Stream(dev)
+def launch_grouped(binding, d, stream):
+    binding.nvfp4_gemm_run_grouped(
+        len(d), [q["A"] for q in d], [q["B"] for q in d], [q["SFA"] for q in d], [q["SFB"] for q in d],
+        [q["C"] for q in d], [q["M"] for q in d], [q["N"] for q in d], [q["K"] for q in d],
+        [q["L"] for q in d], stream)
+
+
+def time_launches(binding, dev_sets, steps, warmup, stream, flush=None):
+    """W eager warm-up launches (they also size the library's per-stream
+    split-K workspace before capture), then K launches replayed from CUDA graphs
+    (one graph per pass over the R input sets, one for the remainder), right
+    after one untimed warm replay.  With `flush` (a buffer larger than L2, for
+    workloads too small to rotate through L2) every step first overwrites the
+    buffer and only the launch itself, between two events, is timed.  Returns
+    (elapsed ms of the K steps, wall-clock start, end)."""
+    sets = len(dev_sets)
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, sets)):
-            launch(dev_sets[i % sets])
+        for i in range(max(warmup, sets)):
+            launch_grouped(binding, dev_sets[i % sets], stream)
     torch.cuda.synchronize()
-    binding.nvfp4_gemm_check_device_status()
-
-    if args.check and rank == 0:
-        import oracle
-        for gi, p in enumerate(host_sets[0]):
-            C = dev_sets[0][gi]["C"]
-            rng = np.random.default_rng(gi)
-            n = 2000
-            ls, ms, ns = rng.integers(0, p["L"], n), rng.integers(0, p["M"], n), rng.integers(0, p["N"], n)
-            ref, absacc = oracle.gemm_points(p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"],
-                                             ls, ms, ns, L=p["L"])
-            g = C[torch.as_tensor(ls), torch.as_tensor(ms), torch.as_tensor(ns)].cpu().numpy()
-            ok, worst, _ = oracle.compare(g, ref, absacc)
-            print("check group %d: ok=%s worst=%.3g" % (gi, ok, worst), file=sys.stderr)
-
-    # ---- the K timed steps are replayed from CUDA graphs (one graph holds one
-    # pass over the R input sets, a second one the remainder), so the host's
-    # launch rate does not limit the device.
-    full, rem = divmod(args.steps, sets)
+    binding.nvfp4_gemm_check_device_status(stream)
+    if flush is not None:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t_wall0 = time.time()
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                launch_grouped(binding, dev_sets[i % sets], stream)
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        binding.nvfp4_gemm_check_device_status(stream)
+        return sum(a.elapsed_time(b) for a, b in ev), t_wall0, t_wall1
+    full, rem = divmod(steps, sets)
     graphs = []
     for count, reps in ((sets, full), (rem, 1)):
         if count == 0 or reps == 0:
@@ -358,88 +356,139 @@ def main():
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(count):
-                launch(dev_sets[i % sets])
+                launch_grouped(binding, dev_sets[i % sets], stream)
         graphs.append((g, reps))
     torch.cuda.synchronize()
-    for g, _ in graphs:          # one untimed replay of each graph
-        g.replay()
-    torch.cuda.synchronize()
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    start_all = torch.cuda.Event(enable_timing=True)
-    end_all = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        start_all.record(stream)
+        for g, _ in graphs:          # warm replay, directly followed by the timed one
+            g.replay()
+        t_wall0 = time.time()
+        e0.record(stream)
         for g, reps in graphs:
             for _ in range(reps):
                 g.replay()
-        end_all.record(stream)
+        e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
-    barrier(world)
-    time.sleep(0.15)
-    clocks = sampler.stop(t_wall0, t_wall1)
     binding.nvfp4_gemm_check_device_status(stream)
-    elapsed_ms = max_over_ranks(start_all.elapsed_time(end_all), world)
-    # back-to-back launches: the average launch duration includes the short
-    # gaps between graph nodes, so it slightly understates the kernel's rate
-    launch_ms = elapsed_ms / args.steps
+    del graphs
+    return e0.elapsed_time(e1), t_wall0, t_wall1
 
-    # ---- repack inside the step (for reference, not the headline)
-    rp_steps = min(args.steps, 2000)
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    raw_sf = []
-    for p in host_sets[0]:
-        raw_sf.append((p["SFA"].to(dev), p["SFB"].to(dev)))
+
+def check_sampled(host0, dev_set):
+    import oracle
+    out = []
+    for gi, p in enumerate(host0):
+        C = dev_set[gi]["C"]
+        rng = np.random.default_rng(gi)
+        n = 2000
+        ls, ms, ns = rng.integers(0, p["L"], n), rng.integers(0, p["M"], n), rng.integers(0, p["N"], n)
+        ref, absacc = oracle.gemm_points(p["A"], p["B"], p["SFA"], p["SFB"], p["M"], p["N"], p["K"],
+                                         ls, ms, ns, L=p["L"])
+        g = C[torch.as_tensor(ls), torch.as_tensor(ms), torch.as_tensor(ns)].cpu().numpy()
+        ok, worst, _ = oracle.compare(g, ref, absacc)
+        out.append({"group": gi, "ok": ok, "worst_ratio": worst})
+    return out
+
+
+def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
+    """Device-timed K steps of one workload with its roofline."""
+    wl = workloads.WORKLOADS[name]
+    sets = max(2, math.ceil(3 * l2 / wl.bytes) + 1)
+    flush = None
+    if sets > 16:
+        # too small to rotate through L2: overwrite a 2 x L2 buffer before every step
+        sets = 2
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        l2_note = "L2 flushed before every step (%.0f MB written), each launch timed alone" % (2 * l2 / 1e6)
+    else:
+        l2_note = "rotating %d input sets, %.0f MB > 3 x L2 (%.0f MB)" % (sets, sets * wl.bytes / 1e6, l2 / 1e6)
+    host0, dev_sets = device_inputs(binding, wl, sets, dev)
+    elapsed_ms, tw0, tw1 = time_launches(binding, dev_sets, args.steps, args.warmup, stream, flush)
+    del flush
+    launch = binding.nvfp4_gemm_last_launch()
+    launch_s = elapsed_ms / args.steps * 1e-3
+    bound, t_hbm, t_fp4, hbm, fp4 = roofline_terms(wl, peaks)
+    if bound == "hbm":
+        achieved, peak, unit = wl.bytes / launch_s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = wl.flops / launch_s / 1e12, fp4, "TFLOP/s"
+    copy_ref = size_matched_copy(wl.bytes, dev, stream, l2) if bound == "hbm" else None
+    res = {
+        "workload": wl.name, "shapes_MNKL": wl.shapes, "steps": args.steps, "warmup": args.warmup,
+        "us_per_launch": launch_s * 1e6, "tflops": wl.flops / launch_s / 1e12,
+        "l2": l2_note,
+        "launch": launch,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": ncu_traffic(wl.name),
+                     "peak_source": "%s (%s)" % (peak_src, "hbm_gbs" if bound == "hbm" else
+                                                 "bf16_tflops x 6 nominal fp4/bf16"),
+                     "algorithmic_bytes_per_launch": wl.bytes, "flops_per_launch": wl.flops,
+                     "avg_launch_us": launch_s * 1e6,
+                     "size_matched_copy": copy_ref,
+                     "frac_of_size_matched_copy": None if copy_ref is None else achieved / copy_ref["achieved"]},
+        "roofline_fraction_min_time": max(t_hbm, t_fp4) / launch_s,
+        "_wall": (tw0, tw1),
+    }
+    if args.check:
+        res["check"] = check_sampled(host0, dev_sets[0])
+    return res, host0, dev_sets
+
+
+def repack_step(binding, host0, dev_sets, steps, dev, stream, wl):
+    """Both scale repacks inside every step, then the GEMM (not the headline)."""
+    sets = len(dev_sets)
+    raw_sf = [(p["SFA"].to(dev), p["SFB"].to(dev)) for p in host0]
     torch.cuda.synchronize()
-    torch.cuda.set_stream(stream)
-    t0e.record(stream)
-    for i in range(rp_steps):
-        d = dev_sets[i % sets]
-        for gi, q in enumerate(d):
-            binding.nvfp4_gemm_repack_scales(raw_sf[gi][0], q["SFA"], q["M"], q["K"], q["L"])
-            binding.nvfp4_gemm_repack_scales(raw_sf[gi][1], q["SFB"], q["N"], q["K"], q["L"])
-        launch(d)
-    t1e.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(steps):
+            d = dev_sets[i % sets]
+            for gi, q in enumerate(d):
+                binding.nvfp4_gemm_repack_scales(raw_sf[gi][0], q["SFA"], q["M"], q["K"], q["L"], stream)
+                binding.nvfp4_gemm_repack_scales(raw_sf[gi][1], q["SFB"], q["N"], q["K"], q["L"], stream)
+            launch_grouped(binding, d, stream)
+        t1.record(stream)
     torch.cuda.synchronize()
-    rp_ms = t0e.elapsed_time(t1e) / rp_steps
+    ms = t0.elapsed_time(t1) / steps
+    return {"value": wl.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps}
 
-    # ---- fused quantize + repack (the step that produces B and SFB) on a
-    # bf16 tensor shaped like group 0's B; larger than L2, so it streams HBM
-    quant = None
-    if not args.no_quantize:
-        q0 = host_sets[0][0]
-        qr, qk, ql = q0["N"], q0["K"], q0["L"]
-        gq = torch.Generator(device=dev).manual_seed(0)
-        xq = torch.randn((ql, qr, qk), device=dev, dtype=torch.float32, generator=gq).to(torch.bfloat16)
-        qcodes = torch.empty((ql, qr, qk // 2), dtype=torch.uint8, device=dev)
-        qsf = torch.empty(binding.nvfp4_gemm_repacked_scales_bytes(qr, qk, ql), dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
-        torch.cuda.synchronize()
-        q_iters = 20
-        t0q, t1q = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0q.record(stream)
-        for _ in range(q_iters):
-            binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
-        t1q.record(stream)
-        torch.cuda.synchronize()
-        q_ms = t0q.elapsed_time(t1q) / q_iters
-        q_bytes = ql * qr * qk * 2 + ql * qr * qk // 2 + qsf.numel()
-        quant = {"shape_LxRxK": [ql, qr, qk], "input": "bf16", "us": q_ms * 1e3,
-                 "algorithmic_bytes": q_bytes, "achieved": q_bytes / (q_ms * 1e-3) / 1e9, "unit": "GB/s"}
-        del xq, qcodes, qsf
 
-    # ---- e2e: host buffers through the C ABI
+def quantize_leg(binding, dev, stream, hbm):
+    """Fused quantize + repack (the step that produces B and SFB) on a bf16
+    tensor shaped like the skinny workload's B (7168 x 16384); larger than L2."""
+    qr, qk, ql = 7168, 16384, 1
+    gq = torch.Generator(device=dev).manual_seed(0)
+    xq = torch.randn((ql, qr, qk), device=dev, dtype=torch.float32, generator=gq).to(torch.bfloat16)
+    qcodes = torch.empty((ql, qr, qk // 2), dtype=torch.uint8, device=dev)
+    qsf = torch.empty(binding.nvfp4_gemm_repacked_scales_bytes(qr, qk, ql), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
+    torch.cuda.synchronize()
+    iters = 20
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(iters):
+            binding.nvfp4_quantize(xq, binding.DTYPE_BF16, qcodes, qsf, qr, qk, ql, stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / iters
+    nbytes = ql * qr * qk * 2 + ql * qr * qk // 2 + qsf.numel()
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"shape_LxRxK": [ql, qr, qk], "input": "bf16", "us": ms * 1e3, "algorithmic_bytes": nbytes,
+            "achieved": ach, "unit": "GB/s", "peak": hbm, "frac": ach / hbm}
+
+
+def e2e_leg(binding, host0, steps, dev, stream, flops):
+    """The metric through the C ABI with host buffers: per step H2D of A, B
+    and the row-major scales from pinned memory, two repacks, the GEMM, D2H of
+    C, all inside the timed region."""
     hp = []
-    h2d = 0
-    d2h = 0
-    for p in host_sets[0]:
+    h2d = d2h = 0
+    for p in host0:
         e = {k: p[k].pin_memory() for k in ("A", "B", "SFA", "SFB")}
         e["Cout"] = torch.empty((p["L"], p["M"], p["N"]), dtype=torch.float16).pin_memory()
         h2d += sum(e[k].numel() * e[k].element_size() for k in ("A", "B", "SFA", "SFB"))
@@ -448,7 +497,7 @@ def main():
 
     def device_buffers():
         out = []
-        for p in host_sets[0]:
+        for p in host0:
             M, N, K, L = p["M"], p["N"], p["K"], p["L"]
             out.append(dict(M=M, N=N, K=K, L=L, A=torch.empty_like(p["A"], device=dev),
                             B=torch.empty_like(p["B"], device=dev), SFAraw=torch.empty_like(p["SFA"], device=dev),
@@ -468,7 +517,7 @@ def main():
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     freed = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step(i):
+    def step(i):
         ed = ed_sets[i % 2]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(freed[i % 2])  # the set's previous step is done with it
@@ -481,85 +530,106 @@ def main():
         stream.wait_event(copied[i % 2])
         with torch.cuda.stream(stream):
             for q in ed:
-                binding.nvfp4_gemm_repack_scales(q["SFAraw"], q["SFA"], q["M"], q["K"], q["L"])
-                binding.nvfp4_gemm_repack_scales(q["SFBraw"], q["SFB"], q["N"], q["K"], q["L"])
-            launch(ed, stream)
+                binding.nvfp4_gemm_repack_scales(q["SFAraw"], q["SFA"], q["M"], q["K"], q["L"], stream)
+                binding.nvfp4_gemm_repack_scales(q["SFBraw"], q["SFB"], q["N"], q["K"], q["L"], stream)
+            launch_grouped(binding, ed, stream)
             for e, q in zip(hp, ed):
                 e["Cout"].copy_(q["C"], non_blocking=True)
             freed[i % 2].record(stream)
 
     for i in range(3):
-        e2e_step(i)
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
     e0.record(stream)
     copy_stream.wait_event(e0)  # no copy of the timed steps starts before the clock does
-    for i in range(args.e2e_steps):
-        e2e_step(i)
+    for i in range(steps):
+        step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
-    binding.nvfp4_gemm_check_device_status()
+    ms = e0.elapsed_time(e1) / steps
+    binding.nvfp4_gemm_check_device_status(stream)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "includes": "H2D of A, B, row-major SFA/SFB; 2 repacks; GEMM; D2H of C; two buffer "
+                        "sets, step i+1's copies overlapping step i"}
 
-    # ---- numbers
-    flops = wl.flops
-    ms_per_step = elapsed_ms / args.steps
-    value = job_throughput(flops, args.steps, elapsed_ms, world)
+
+# ------------------------------------------------------------------ our arm
+def main(argv=None):
+    args = parse(argv)
+    if one_gpu_only(args):
+        return
+    if args.impl == "reference":
+        return run_reference(args)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from block_scaled_fp4_nvfp4_gb300 import binding
+    binding.load_library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
     peaks, peak_src = load_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    fp4_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * FP4_OVER_BF16
-    t_hbm = wl.bytes / (hbm * 1e9)
-    t_fp4 = flops / (fp4_peak * 1e12)
-    bound = "hbm" if t_hbm >= t_fp4 else "tensor"
-    launch_s = launch_ms * 1e-3
-    if bound == "hbm":
-        achieved, peak, unit = wl.bytes / launch_s / 1e9, hbm, "GB/s"
-    else:
-        achieved, peak, unit = flops / launch_s / 1e12, fp4_peak, "TFLOP/s"
+    stream = torch.cuda.Stream(dev)
 
-    copy_ref = size_matched_copy(wl.bytes, dev, stream, l2) if bound == "hbm" else None
+    if args.configs == "all":
+        configs = list(workloads.WORKLOAD_ORDER)
+    elif args.configs == "none":
+        configs = []
+    else:
+        configs = [c for c in args.configs.split(",") if c]
+    if args.workload not in configs:
+        configs.append(args.workload)
+
+    sampler = ClockSampler(0)
+    sampler.start()
+    per_config = {}
+    head = head_inputs = None
+    for name in configs:
+        res, host0, dev_sets = measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src)
+        per_config[name] = res
+        if name == args.workload:
+            head, head_inputs = res, (host0, dev_sets)
+        else:
+            del dev_sets
+        torch.cuda.empty_cache()
+    wl = workloads.WORKLOADS[args.workload]
+
+    extra = {}
+    host0, dev_sets = head_inputs
+    if not args.no_repack_step:
+        extra["step_with_repack"] = repack_step(binding, host0, dev_sets, min(args.steps, 200), dev, stream, wl)
+    del dev_sets
+    torch.cuda.empty_cache()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    extra["quantize"] = None if args.no_quantize else quantize_leg(binding, dev, stream, hbm)
+    e2e = e2e_leg(binding, host0, args.e2e_steps, dev, stream, wl.flops)
+    sampler.stop()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         v, dt, threads, desc = time_oracle(args.workload, args.cpu_seconds)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc + ", %.1f s" % dt}
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
-            "config": {"workload": wl.name, "shapes_MNKL": wl.shapes, "seed": 0,
-                       "l2": "rotating %d input sets, %.0f MB > 3 x L2 (%.0f MB)" % (
-                           sets, sets * wl.bytes / 1e6, l2 / 1e6),
-                       "parallelism": "replica per GPU" if world > 1 else "single GPU"},
-            "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                         "frac": achieved / peak, "traffic": ncu_traffic(wl.name),
-                         "peak_source": "%s (%s)" % (peak_src, "hbm_gbs" if bound == "hbm" else
-                                                     "bf16_tflops x 6 nominal fp4/bf16"),
-                         "algorithmic_bytes_per_launch": wl.bytes, "flops_per_launch": flops,
-                         "avg_launch_us": launch_ms * 1e3,
-                         "size_matched_copy": copy_ref,
-                         "frac_of_size_matched_copy": None if copy_ref is None else achieved / copy_ref["achieved"]},
-            "roofline_fraction_min_time": max(t_hbm, t_fp4) / launch_s,
-            "cpu_baseline": cpu,
-            "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "ms_per_step": e2e_ms, "steps": args.e2e_steps, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "includes": "H2D of A, B, row-major SFA/SFB; 2 repacks; GEMM; D2H of C; two buffer "
-                                "sets, step i+1's copies overlapping step i"},
-            "step_with_repack": {"value": flops / (rp_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                                 "ms_per_step": rp_ms},
-            "quantize": None if quant is None else dict(quant, peak=hbm, frac=quant["achieved"] / hbm),
-            "gpu_launches": args.steps,
-            "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    # clocks of each timed region (the sampler ran across all of them)
+    for res in per_config.values():
+        res["clocks"] = sampler.window(*res.pop("_wall"))
+    line = {
+        "metric": METRIC, "value": head["tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["us_per_launch"] / 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4", "data": "synthetic",
+        "config": {"workload": wl.name, "shapes_MNKL": wl.shapes, "seed": 0, "l2": head["l2"],
+                   "parallelism": "single GPU"},
+        "roofline": head["roofline"],
+        "roofline_fraction_min_time": head["roofline_fraction_min_time"],
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": head["clocks"],
+        "per_config": {n: {k: v for k, v in r.items() if k not in ("workload",)} for n, r in per_config.items()},
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -502,6 +502,26 @@ int launch_mode(const Plan& pl) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every buffer must be memory of the current device (device or managed
+// allocation): the kernels read operands through tensor maps, some of them
+// delivering one load to both CTAs of a cluster, and write C through tensor
+// maps as well; a host pointer or another GPU's memory reached through the
+// unified address space is refused before anything is encoded or launched.
+int check_local(const void* p, int dev, const char* what, int g) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // reset the runtime's last-error state this call set
+    return fail(NVFP4_ERR_INVALID_ARG, "group %d: %s (%p) is not a CUDA allocation: %s", g, what, p,
+                cudaGetErrorString(e));
+  }
+  if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != dev)
+    return fail(NVFP4_ERR_INVALID_ARG,
+                "group %d: %s (%p) is not device memory of the current device %d (memory type %d, device %d)",
+                g, what, p, dev, static_cast<int>(a.type), a.device);
+  return NVFP4_OK;
+}
+
 int check_shapes(int G, const int* M, const int* N, const int* K, const int* L) {
   if (G < 1 || G > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_INVALID_ARG, "G=%d outside 1..%d", G, NVFP4_MAX_GROUPS);
   if (!M || !N || !K || !L) return fail(NVFP4_ERR_INVALID_ARG, "null size array");
@@ -555,6 +575,10 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t cou
   return NVFP4_OK;
 }
 
+// Reads and clears the status word of the no-allocation variant's static
+// area on device `dev` (defined with that area at the end of this file).
+int noalloc_take_status(int dev, int* status);
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -571,7 +595,13 @@ int nvfp4_gemm_repack_scales(const void* sf, void* out, int rows, int K, int L, 
   if (!aligned16(sf) || !aligned16(out)) return fail(NVFP4_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
   if (rows < 1 || K < 16 || L < 1 || K % 16 != 0)
     return fail(NVFP4_ERR_INVALID_ARG, "bad sizes rows=%d K=%d L=%d (K %% 16 == 0 required)", rows, K, L);
-  cudaError_t e = repack_launch(sf, out, rows, K, L, static_cast<cudaStream_t>(stream));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int rc;
+  if ((rc = check_local(sf, dev, "sf", 0)) != NVFP4_OK || (rc = check_local(out, dev, "out", 0)) != NVFP4_OK)
+    return rc;
+  e = repack_launch(sf, out, rows, K, L, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "repack launch");
   return ok();
 }
@@ -588,6 +618,12 @@ int nvfp4_quantize(const void* x, int x_dtype, void* codes, void* sf_repacked, i
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  {
+    int rc;
+    if ((rc = check_local(x, dev, "x", 0)) != NVFP4_OK || (rc = check_local(codes, dev, "codes", 0)) != NVFP4_OK ||
+        (rc = check_local(sf_repacked, dev, "sf_repacked", 0)) != NVFP4_OK)
+      return rc;
+  }
   const int is_f16 = x_dtype == NVFP4_DTYPE_F16 ? 1 : 0;
   int max_blocks = 0;
   {
@@ -624,6 +660,12 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   DeviceState* ds = nullptr;
   if ((rc = device_state(dev, &ds)) != NVFP4_OK) return rc;
+  for (int g = 0; g < G; ++g) {
+    if ((rc = check_local(A[g], dev, "A", g)) != NVFP4_OK || (rc = check_local(B[g], dev, "B", g)) != NVFP4_OK ||
+        (rc = check_local(SFA[g], dev, "SFA", g)) != NVFP4_OK || (rc = check_local(SFB[g], dev, "SFB", g)) != NVFP4_OK ||
+        (rc = check_local(C[g], dev, "C", g)) != NVFP4_OK)
+      return rc;
+  }
 
   Plan pl;
   if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl)) != NVFP4_OK) return rc;
@@ -720,6 +762,10 @@ int nvfp4_gemm_check_device_status(void* stream_) {
   int h = 0;
   if ((e = cudaMemcpy(&h, ds->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy(status)");
+  // the no-allocation variant's launches record into their own static word
+  int h_noalloc = 0;
+  if ((rc = noalloc_take_status(dev, &h_noalloc)) != NVFP4_OK) return rc;
+  if (h == 0) h = h_noalloc;
   if (h != 0) {
     // An aborted launch may leave split-K arrival counters non-zero: clear
     // every workspace of this device before reporting.
@@ -816,8 +862,9 @@ uint64_t nvfp4_gemm_encode_smem_desc(uint32_t smem_addr, int swizzle128) {
 namespace {
 
 // Largest stream-K partial area the static array holds: 256 partial tiles of
-// 128 x 128 fp32 (16 MiB), e.g. the 56 tiles x 4 segments of a
-// 128 x 7168 x 16384 problem on 152 SMs.
+// 128 x 128 fp32 (16 MiB).  A 128 x 7168 x 16384 problem on 148-152 SMs plans
+// 56 tiles x 2 segments (112 partial tiles, 7.3 MiB); plans needing more than
+// 256 partial tiles are refused.
 constexpr size_t kNoAllocPartialBytes = 256ull * kBM * 128 * sizeof(float);  // 16 MiB
 constexpr int kNoAllocCounters = 4096;       // output tiles of one split launch
 constexpr size_t kNoAllocHeader = 256;       // status word, padded
@@ -863,6 +910,18 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
   return NVFP4_OK;
 }
 
+int noalloc_take_status(int dev, int* status) {
+  *status = 0;
+  auto it = g_noalloc_devices.find(dev);
+  if (it == g_noalloc_devices.end() || !it->second.ready) return NVFP4_OK;  // never launched here
+  cudaError_t e;
+  if ((e = cudaMemcpy(status, it->second.scratch, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(no-allocation status)");
+  if (*status != 0 && (e = cudaMemset(it->second.scratch, 0, sizeof(int))) != cudaSuccess)
+    return cuda_fail(e, "cudaMemset(no-allocation status)");
+  return NVFP4_OK;
+}
+
 }  // namespace
 
 extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* SFA, const void* SFB,
@@ -880,6 +939,10 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   NoAllocDevice* nd = nullptr;
   if ((rc = noalloc_setup(dev, &nd)) != NVFP4_OK) return rc;
+  if ((rc = check_local(A, dev, "A", 0)) != NVFP4_OK || (rc = check_local(B, dev, "B", 0)) != NVFP4_OK ||
+      (rc = check_local(SFA, dev, "SFA", 0)) != NVFP4_OK || (rc = check_local(SFB, dev, "SFB", 0)) != NVFP4_OK ||
+      (rc = check_local(C, dev, "C", 0)) != NVFP4_OK)
+    return rc;
 
   Plan pl;
   if ((rc = make_plan(1, &M, &N, &K, &L, nd->sms, &pl, /*allow_cluster=*/false)) != NVFP4_OK) return rc;
@@ -903,18 +966,23 @@ extern "C" int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* 
   p.a_streams[0] = M > N ? 1 : 0;
   p.sched = pl.sched;
   p.timeout_ns = g_timeout_ns.load();
-  p.debug_skip_ktile = -1;
+  p.debug_skip_ktile = g_debug_skip.exchange(-1);
   p.status = reinterpret_cast<int*>(nd->scratch);
   p.counters = reinterpret_cast<int*>(nd->scratch + kNoAllocHeader);
   p.workspace = reinterpret_cast<float*>(nd->scratch + kNoAllocHeader + kNoAllocCounterBytes);
 
-  // The array keeps whatever the previous call left: the status word and the
-  // counters this launch uses must start at zero (the partial tiles are always
-  // written before they are read).
-  const size_t clear = kNoAllocHeader + static_cast<size_t>(pl.counters) * sizeof(int);
-  if ((e = cudaMemsetAsync(nd->scratch, 0, clear, stream)) != cudaSuccess)
-    return cuda_fail(e, "cudaMemsetAsync(no-allocation scratch)");
-  e = gemm_launch(pl.bn, 1, kModeSingle, p, pl.grid, stream, false);  // follows a memset: plain launch
+  // The array keeps whatever the previous call left.  The tile counters this
+  // launch uses must start at zero (an aborted launch may leave some set); the
+  // partial tiles are always written before they are read; the status word
+  // (zero when the library is loaded) keeps a timeout until
+  // nvfp4_gemm_check_device_status reads and clears it.
+  if (pl.counters > 0) {
+    const size_t clear = static_cast<size_t>(pl.counters) * sizeof(int);
+    if ((e = cudaMemsetAsync(nd->scratch + kNoAllocHeader, 0, clear, stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(no-allocation counters)");
+  }
+  // after a memset, a plain launch (no programmatic overlap with it)
+  e = gemm_launch(pl.bn, 1, kModeSingle, p, pl.grid, stream, pl.counters == 0);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
   g_last_launch[0] = pl.bn;
   g_last_launch[1] = pl.grid;

@@ -24,6 +24,9 @@
  *   - All pointers named "device" are device pointers on the current CUDA
  *     device; the caller owns them and keeps them alive until the work queued
  *     on `stream` has finished.  Host arrays are read before the call returns.
+ *     Every device pointer is checked with cudaPointerGetAttributes: host
+ *     memory (pinned or not) and memory of another GPU are refused with
+ *     NVFP4_ERR_INVALID_ARG before anything is launched.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  All work is asynchronous on that stream; nothing synchronises
  *     unless stated.
@@ -154,8 +157,10 @@ NVFP4_API const char* nvfp4_gemm_last_error_string(void);
  * frees its tensor memory and returns.  Its output is then undefined.
  *
  * nvfp4_gemm_check_device_status synchronises `stream`, reads and clears the
- * current device's status word and returns NVFP4_OK or
+ * current device's status words (the one of nvfp4_gemm_run / _run_grouped
+ * and the one of nvfp4_gemm_run_noalloc) and returns NVFP4_OK or
  * NVFP4_ERR_DEVICE_TIMEOUT (or CUDA if the synchronisation itself failed).
+ * It makes no device allocation.
  */
 NVFP4_API int nvfp4_gemm_check_device_status(void* stream);
 
@@ -230,16 +235,17 @@ NVFP4_API int nvfp4_gemm_last_launch(int* out, int out_len);
  * every device which loads this library holds until the process exits.  The
  * first call on a device (with that device current) looks up the array's
  * device address once; make that first call before capturing any stream.
- * Each call clears the counters and status word it uses (an asynchronous
- * memset on `stream`) and calls no allocator.
+ * Each call clears the tile counters it uses (an asynchronous memset on
+ * `stream`) and calls no allocator.
  *
  * All calls share the one array: calls whose work may overlap on the GPU
  * (different streams, or different host threads) race on it and give wrong
  * results; order them on one stream.  A problem whose stream-K plan needs more
  * than the array holds returns NVFP4_ERR_UNSUPPORTED_SHAPE with the sizes in
  * the error string.  A bounded device wait that runs out ends the kernel early
- * and leaves C undefined; in this variant the timeout is recorded only in the
- * array's own status word, which the next call clears.
+ * and leaves C undefined; the timeout stays in the array's status word until
+ * nvfp4_gemm_check_device_status (which reads both status words of the
+ * current device) reports and clears it.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, UNSUPPORTED_DEVICE, CUDA.
  */
 NVFP4_API int nvfp4_gemm_run_noalloc(const void* A, const void* B, const void* SFA, const void* SFB,

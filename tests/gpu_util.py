@@ -1,5 +1,11 @@
 """Helpers shared by the GPU tests: build/load the library once, move a seeded
-problem to the device, run it through the C ABI, compare with the oracle."""
+problem to the device, run it through the C ABI, compare with the oracle.
+
+Every oracle comparison records the worst |gpu - ref| / tolerance it saw, per
+test; the session summary (tests/conftest.py) prints the largest ones, so a
+kernel drifting towards the bound shows before it crosses it."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -7,6 +13,14 @@ import torch
 import oracle
 
 _built = False
+
+# (test id, what was compared, elements, worst ratio) of every comparison
+WORST_RATIOS = []
+
+
+def record_worst(worst, n, what):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").rsplit(" (", 1)[0]
+    WORST_RATIOS.append((test, what, int(n), float(worst)))
 
 
 def ensure_built():
@@ -59,6 +73,7 @@ def assert_close_full(gpu_c, p):
     g = gpu_c.detach().cpu().numpy()
     assert not np.isnan(g).any(), "unwritten output elements"
     ok, worst, idx = oracle.compare(g, ref, absacc)
+    record_worst(worst, g.size, "full")
     assert ok, "worst |err|/tol = %.4g at flat index %d (gpu %r ref %r)" % (
         worst, idx, g.ravel()[idx], ref.ravel()[idx])
     return worst
@@ -89,6 +104,7 @@ def assert_close_points(gpu_c, p, ls, ms, ns):
     g = gpu_c.detach()[torch.as_tensor(ls), torch.as_tensor(ms), torch.as_tensor(ns)].cpu().numpy()
     assert not np.isnan(g).any(), "unwritten output elements"
     ok, worst, idx = oracle.compare(g, ref, absacc)
+    record_worst(worst, g.size, "points")
     assert ok, "worst |err|/tol = %.4g at point (%d,%d,%d): gpu %r ref %r" % (
         worst, ls[idx], ms[idx], ns[idx], g[idx], ref[idx])
     return worst
