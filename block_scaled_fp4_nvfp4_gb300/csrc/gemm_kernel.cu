@@ -1,17 +1,18 @@
 // Persistent, warp-specialised NVFP4 block-scaled GEMM for sm_103a.
 //
 // One CTA per SM walks a static list of work units (output tile, K range) of
-// all groups.  Inside a CTA (224 threads):
-//   warps 0-1   TMA producers: per 256-wide k-tile warp 0 arms the stage's
+// all groups.  Inside a CTA (256 threads):
+//   warps 0-2   TMA producers: per 256-wide k-tile warp 0 arms the stage's
 //               "full" mbarrier and copies the A tile (128 rows x 128 B) and
 //               its scale slab, warp 1 the B tile (BN rows x 128 B, or this
-//               CTA's half of it when two CTAs share it) and its scale slabs;
-//   warp 2      MMA issuer (one elected lane): per MMA k-block its scale atoms
+//               CTA's half of it when two CTAs share it), warp 2 the B scale
+//               slabs;
+//   warp 3      MMA issuer (one elected lane): per MMA k-block its scale atoms
 //               into tensor memory with tcgen05.cp, then one
 //               tcgen05.mma.kind::mxf4nvf4.block_scale.block16 (128 x BN x 64,
 //               or 256 x BN x 64 over a CTA pair) into a tensor-memory
 //               accumulator; one commit per k-tile frees the stage;
-//   warps 3-6   epilogue, one per 32-lane tensor-memory sub-partition:
+//   warps 4-7   epilogue, one per 32-lane tensor-memory sub-partition:
 //               tcgen05.ld of the accumulator (one row per thread), fp32 ->
 //               fp16 (RNE), 64B-swizzled staging and TMA stores of 32 x 32
 //               boxes (rows past M and columns past N are clipped).
@@ -57,6 +58,18 @@ struct SmemCtl {
   uint32_t tmem_base;
   volatile int abort;
   int last_flag;
+  // Copy bookkeeping for the drain after an abort: per producer warp and
+  // stage, the last use (the warp's k-tile count) it issued copies for and
+  // the bytes those copies deliver to each destination barrier; warp 0's
+  // arming of each stage (use and armed byte count); in reduce clusters,
+  // whether red_full was armed and which ranks this CTA's partial went to.
+  int rec_use[kProducerWarps][kMaxStages];
+  uint32_t rec_bytes[kProducerWarps][kMaxStages];
+  int arm_use[kMaxStages];
+  uint32_t arm_bytes[kMaxStages];
+  int red_armed;
+  uint32_t red_sent;
+  uint32_t peer_abort[4];  // abort flags the cluster's CTAs published here (index = rank)
 };
 
 // Bounded mbarrier wait.  Returns false if the CTA is aborting or the limit
@@ -189,6 +202,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::mbar_init(ptx::smem_addr(&ctl.red_full), 1);  // armed with the peers' bytes
     ctl.abort = 0;
     ctl.last_flag = 0;
+    for (int s = 0; s < kMaxStages; ++s) {
+      for (int w = 0; w < kProducerWarps; ++w) {
+        ctl.rec_use[w][s] = -1;
+        ctl.rec_bytes[w][s] = 0;
+      }
+      ctl.arm_use[s] = -1;
+      ctl.arm_bytes[s] = 0;
+    }
+    ctl.red_armed = 0;
+    ctl.red_sent = 0;
+    for (int r = 0; r < 4; ++r) ctl.peer_abort[r] = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -218,9 +242,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
   const uint32_t tmem = ctl.tmem_base;
 
   // Programmatic dependent launch: everything above overlaps the previous
-  // kernel on the stream.  Optionally (prefetch_ktiles > 0) one thread asks L2
-  // for the first k-tiles this CTA will load before waiting for it; every
-  // actual load and store comes after the wait.
+  // kernel on the stream, and so does each role's set-up below (its work
+  // list, the first tile's addresses -- loads from the parameter block whose
+  // latency would otherwise sit between the previous kernel's end and the
+  // first copy).  Only global memory must wait for the previous kernel: the
+  // producers wait right before their first copy and the epilogue before its
+  // first store; the MMA warp touches shared and tensor memory only and never
+  // waits.  Optionally (prefetch_ktiles > 0) one thread asks L2 for the first
+  // k-tiles this CTA will load before that wait.
   if (warp == 0 && lane == 0 && p.prefetch_ktiles > 0) {
     WorkCursor pc;
     work_begin(p.sched, unit, units, pc, wrank);
@@ -239,30 +268,94 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       }
     }
   }
-  ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
   const Waiter W{&ctl.abort, p.status, p.timeout_ns};
 
+  // Counted drain after an abort, run by one thread of each CTA once every
+  // warp of the cluster has stopped issuing.  For each stage it takes the last
+  // use any producer warp issued copies for (its own warps' and, where copies
+  // signal this CTA's barrier from the peer -- B multicast, 2-SM pairs -- the
+  // peer's records, read through distributed shared memory).  If that phase
+  // is still open it makes the phase completable by exactly the bytes that
+  // were issued: it adds the arrival and byte count warp 0 did not make, or
+  // counts as done the bytes armed for but never issued; then it waits
+  // (bounded) for the phase, i.e. for every issued copy to have landed.  The
+  // reduction clusters' partial exchange is drained the same way.
+  auto drain_after_abort = [&]() {
+    auto peer_word = [&](const void* local, int rank) {
+      return ptx::ld_shared_cluster(ptx::mapa_shared(ptx::smem_addr(local), static_cast<uint32_t>(rank)));
+    };
+    if (!P2 || crank == 0) {  // a pair's copies all signal the leader's barriers
+      for (int s = 0; s < kStages; ++s) {
+        int use = ctl.arm_use[s];
+        for (int w = 0; w < kProducerWarps; ++w) use = ctl.rec_use[w][s] > use ? ctl.rec_use[w][s] : use;
+        int peer_use[kProducerWarps];
+        uint32_t peer_bytes[kProducerWarps];
+        for (int w = 0; w < kProducerWarps; ++w) {
+          peer_use[w] = -1;
+          peer_bytes[w] = 0;
+          if ((P2 || (kMc && w > 0)) && CL == 2) {  // peer warps whose copies land here
+            peer_use[w] = static_cast<int>(peer_word(&ctl.rec_use[w][s], crank ^ 1));
+            peer_bytes[w] = peer_word(&ctl.rec_bytes[w][s], crank ^ 1);
+            use = peer_use[w] > use ? peer_use[w] : use;
+          }
+        }
+        if (use < 0) continue;
+        const uint32_t parity = static_cast<uint32_t>(use / kStages) & 1u;
+        const uint32_t bar = full_bar(s);
+        if (ptx::mbar_try_wait(bar, parity)) continue;  // complete: nothing of it in flight
+        uint32_t issued = 0;
+        for (int w = 0; w < kProducerWarps; ++w) {
+          if (ctl.rec_use[w][s] == use) issued += ctl.rec_bytes[w][s];
+          if (peer_use[w] == use) issued += peer_bytes[w];
+        }
+        if (ctl.arm_use[s] == use) {
+          if (ctl.arm_bytes[s] > issued) ptx::mbar_complete_tx(bar, ctl.arm_bytes[s] - issued);
+        } else {
+          ptx::mbar_arrive_expect_tx(bar, issued);
+        }
+        W.drain(bar, parity);
+      }
+    }
+    if constexpr (kRed) {
+      constexpr uint32_t kSlotBytes = BN / CL * kBM * 4;
+      uint32_t got = 0;
+      for (int r = 0; r < CL; ++r)
+        if (r != crank && ((peer_word(&ctl.red_sent, r) >> crank) & 1u)) got += kSlotBytes;
+      const uint32_t bar = ptx::smem_addr(&ctl.red_full);
+      if ((ctl.red_armed || got) && !ptx::mbar_try_wait(bar, 0)) {
+        const uint32_t expected = (CL - 1) * kSlotBytes;
+        if (ctl.red_armed) {
+          if (expected > got) ptx::mbar_complete_tx(bar, expected - got);
+        } else {
+          ptx::mbar_arrive_expect_tx(bar, got);
+        }
+        W.drain(bar, 0);
+      }
+    }
+  };
+
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
-    // Two producer warps fill every stage together: warp 0 arms the stage's
+    // Three producer warps fill every stage together: warp 0 arms the stage's
     // barrier with the whole byte count and loads A and its scales, warp 1
-    // loads B and its scales.  Splitting the copies halves the time from a
-    // stage's release to its refill, which bounds the ring's throughput (the
-    // barrier's byte count may briefly go negative when warp 1's bytes land
-    // first; the phase still needs warp 0's arrival).  Within a warp every lane
-    // runs the loop with warp-uniform values and one elected lane issues each
-    // copy (see the *_elect wrappers).
+    // loads B, warp 2 the B scale slabs.  Splitting the copies shortens the
+    // time from a stage's release to its refill, which bounds the ring's
+    // throughput (the barrier's byte count may briefly go negative when
+    // another warp's bytes land first; the phase still needs warp 0's
+    // arrival).  Measured on GB300 against two warps (B and its slabs on one):
+    // 8192^3 as 2-SM pairs 177 -> 172 us, the two-group workload 27.7 -> 27.4
+    // us, the others unchanged.  Within a warp every lane runs the loop with
+    // warp-uniform values and one elected lane issues each copy (see the
+    // *_elect wrappers).
     const uint64_t pol_stream = ptx::policy_evict_first();
     const uint64_t pol_keep = ptx::policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
-    int armed[kStages];
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) armed[s] = -1;
     int count = 0;
     bool ok = true;
+    bool dep_done = false;  // griddepcontrol.wait passed
     WorkCursor cur;
     work_begin(p.sched, unit, units, cur, wrank);
     Work x;
@@ -293,8 +386,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         const uint32_t sB = sA + Cfg::kABytes;
         const uint32_t sSFA = sB + Cfg::kBBytes;
         const uint32_t sSFB = sSFA + kSfSlabBytes;
+        if (!dep_done) {
+          ptx::griddep_wait();  // the previous kernel's writes are visible from here on
+          dep_done = true;
+        }
         if (blockIdx.x == 0 && count == p.debug_skip_ktile) {
-          armed[stage] = -1;  // test-only: nothing issued, nothing in flight
+          // test-only: nothing issued, nothing in flight, nothing recorded
         } else {
           const uint32_t fb = full_bar(stage);
           if constexpr (P2) {
@@ -308,8 +405,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
               if (crank == 0) ptx::mbar_arrive_expect_tx_elect(fb, 2u * Cfg::kStageBytes);
               ptx::tma_load_3d_pair_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, lfb, polA);
               ptx::tma_load_2d_pair_elect(sSFA, &p.tmSFA[x.g], 0, sfa_row + kt * 8, lfb, polA);
-            } else {
+            } else if (warp == 1) {
               ptx::tma_load_3d_pair_elect(sB, mapB, kt * kBKBytes, x.tn * BN + crank * kBHalfRows, x.l, lfb, polB);
+            } else {
 #pragma unroll
               for (int j = 0; j < Cfg::kSfbBlocks; ++j)
                 ptx::tma_load_2d_pair_elect(sSFB + j * kSfSlabBytes, &p.tmSFB[x.g], 0,
@@ -321,21 +419,48 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
             ptx::tma_load_3d_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, fb, polA);
             ptx::bulk_load_elect(sSFA, sfa + static_cast<size_t>(kt) * kSfSlabBytes, kSfSlabBytes, fb, polA);
           } else if constexpr (!kMc) {
-            ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
-            for (int j = 0; j < nsfb; ++j)
-              ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
-                                   sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
-                                   kSfSlabBytes, fb, polB);
-          } else {
-            // this CTA's half of the B rows and every CL-th scale slab, for both CTAs
+            if (warp == 1) {
+              ptx::tma_load_3d_elect(sB, mapB, kt * kBKBytes, x.tn * BN, x.l, fb, polB);
+            } else {
+              for (int j = 0; j < nsfb; ++j)
+                ptx::bulk_load_elect(sSFB + j * kSfSlabBytes,
+                                     sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
+                                     kSfSlabBytes, fb, polB);
+            }
+          } else if (warp == 1) {
+            // this CTA's half of the B rows, for both CTAs
             ptx::tma_load_3d_mc_elect(sB + crank * kBHalfRows * kBKBytes, mapB, kt * kBKBytes,
                                       x.tn * BN + crank * kBHalfRows, x.l, fb, polB, kPeers);
+          } else {
+            // every CL-th B scale slab, for both CTAs
             for (int j = crank; j < nsfb; j += CL)
               ptx::bulk_load_mc_elect(sSFB + j * kSfSlabBytes,
                                       sfb + (static_cast<size_t>(j) * atoms_per_block + kt * 4) * kSfAtomBytes,
                                       kSfSlabBytes, fb, polB, kPeers);
           }
-          armed[stage] = static_cast<int>(phase);
+          // Record what went out (every lane stores the same values: no
+          // divergent branch in the issue loop).  Bytes are counted as each
+          // destination barrier sees them: a multicast copy delivers its full
+          // size to every CTA of the cluster.
+          uint32_t sent;
+          if (warp == 0) {
+            sent = Cfg::kABytes + kSfSlabBytes;
+            const bool arms = !P2 || crank == 0;
+            if (arms) {
+              ctl.arm_use[stage] = count;
+              ctl.arm_bytes[stage] = P2 ? 2u * Cfg::kStageBytes : stage_tx;
+            }
+          } else if (warp == 1) {
+            sent = static_cast<uint32_t>(kBHalfRows) * kBKBytes;
+          } else if constexpr (P2) {
+            sent = Cfg::kSfbBlocks * kSfSlabBytes;
+          } else if constexpr (kMc) {
+            sent = static_cast<uint32_t>(nsfb > crank ? (nsfb - crank + CL - 1) / CL : 0) * kSfSlabBytes;
+          } else {
+            sent = static_cast<uint32_t>(nsfb) * kSfSlabBytes;
+          }
+          ctl.rec_use[warp][stage] = count;
+          ctl.rec_bytes[warp][stage] = sent;
         }
         ++count;
         if (++stage == kStages) {
@@ -344,17 +469,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         }
       }
     }
-    if (!ok && (!P2 || crank == 0)) {
-      // Shutting down: wait for the copies this warp put in flight.  (A pair's
-      // odd CTA cannot wait on the leader's barriers; it lingers before
-      // exiting instead, see the end of the kernel.)
-      if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-          if (armed[s] >= 0) W.drain(full_bar(s), static_cast<uint32_t>(armed[s]));
-      }
-      __syncwarp();
-    }
+    // After an abort the copies still in flight are waited for at the end
+    // of the kernel, from the records above (drain_after_abort).
   } else if (warp == kMmaWarp && (!P2 || crank == 0)) {
     // ------------------------------------------------------------ MMA issuer
     // Whole warp in the loop, one elected lane issues every tcgen05 operation
@@ -457,6 +573,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     }
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue
+    ptx::griddep_wait();  // before any store or workspace access
     const int ew = warp - kFirstEpiWarp;  // epilogue warp 0..3
     const int sub = warp & 3;          // tensor-memory sub-partition this warp may read
     const int row = sub * 32 + lane;   // tile row owned by this thread
@@ -512,6 +629,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     work_begin(p.sched, unit, units, cur, wrank);
     Work x;
     while (work_next(p.sched, unit, units, cur, x)) {
+      // This CTA's last work item?  Once its accumulator is complete every
+      // MMA of the CTA (and of its cluster peer's shared tiles) has read its
+      // stage, and no copy will land in the ring again.
+      WorkCursor peek = cur;
+      Work next_x;
+      const bool last_item = !work_next(p.sched, unit, units, peek, next_x);
       if (!warp_wait(W, acc_full_bar(ab), aphase, kStatusTimeoutEpilogue)) break;
       ptx::tc_fence_after_sync();
       const uint32_t t_row = tmem + (static_cast<uint32_t>(sub * 32) << 16) + ab * BN;
@@ -558,8 +681,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         }
         release_acc();
         if (rows_live) {
+          if (last_item) {
+            // The ring is idle: every box gets its own staging buffer there, so
+            // the warp's stores go out back to back instead of each waiting for
+            // the previous one to leave the warp's single buffer (the last
+            // tile's epilogue is the kernel's tail).
+            static_assert(kEpiWarps * (BN / 32) * Cfg::kEpiBufBytes <= kStages * Cfg::kStageBytes,
+                          "final staging exceeds the ring");
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) store_box(x, 32 * c, &h[16 * c]);
+            for (int c = 0; c < BN / 32; ++c)
+              stage_and_store(x, 32 * c, &h[16 * c], smem_base + (ew * (BN / 32) + c) * Cfg::kEpiBufBytes);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) store_box(x, 32 * c, &h[16 * c]);
+          }
         }
         continue;
       }
@@ -595,7 +730,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // This CTA's MMAs are complete (acc_full), so its ring may be
         // written: tell every CTA of the cluster.
         if (ew == 0 && lane < CL) ptx::mbar_arrive_remote(ptx::mapa_shared(go_bar, static_cast<uint32_t>(lane)));
-        if (ew == 0 && lane == 0) ptx::mbar_arrive_expect_tx(rfull_bar, (CL - 1) * kSlotBytes);
+        if (ew == 0 && lane == 0) {
+          ptx::mbar_arrive_expect_tx(rfull_bar, (CL - 1) * kSlotBytes);
+          ctl.red_armed = 1;
+        }
         uint32_t slot[CL];
 #pragma unroll
         for (int r = 0; r < CL; ++r)
@@ -623,10 +761,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           if (lane == 0) {
 #pragma unroll
             for (int r = 0; r < CL; ++r)
-              if (r != static_cast<int>(crank))
+              if (r != static_cast<int>(crank)) {
                 ptx::bulk_copy_to_cluster(ptx::mapa_shared(smem_base + crank * kSlotBytes, static_cast<uint32_t>(r)),
                                           smem_base + static_cast<uint32_t>(CL + r) * kSlotBytes, kSlotBytes,
                                           ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
+                ctl.red_sent |= 1u << r;
+              }
           }
           __syncwarp();
         }
@@ -759,23 +899,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
 
   ptx::tc_fence_before_sync();
   __syncthreads();
-  if constexpr (P2 || kRed) {
-    // After an abort a pair CTA may still have copies in flight that only the
-    // leader's barriers count, and a cluster-reduction CTA may still be the
-    // source or target of a bulk copy: give them time to land before the
-    // shared memory goes away (plain copies; microseconds).
-    if (ctl.abort) {
-      if (threadIdx.x == 0) {
-        const uint64_t t0 = ptx::globaltimer();
-        while (ptx::globaltimer() - t0 < 200000ull) {
-        }
-      }
-      __syncthreads();
-    }
+  // No CTA leaves while a peer may still multicast into its shared memory or
+  // signal its barriers.  Every CTA publishes its abort flag to all CTAs of
+  // the cluster before the barrier, so the decision to drain below is the
+  // same in every CTA.
+  bool drain = ctl.abort != 0;
+  if constexpr (CL > 1) {
+    if (threadIdx.x < CL)
+      ptx::st_shared_cluster(ptx::mapa_shared(ptx::smem_addr(&ctl.peer_abort[crank]), threadIdx.x),
+                             static_cast<uint32_t>(ctl.abort));
+    ptx::cluster_sync();
+#pragma unroll
+    for (int r = 0; r < CL; ++r) drain = drain || ctl.peer_abort[r] != 0;
   }
-  // No CTA leaves while its peer may still multicast into its shared memory
-  // or signal its barriers.
-  if constexpr (CL > 1) ptx::cluster_sync();
+  if (drain) {
+    // After an abort, copies may still be in flight into this CTA's shared
+    // memory: wait for them, counted, before it is released.
+    if (threadIdx.x == 0) drain_after_abort();
+    __syncthreads();
+    if constexpr (CL > 1) ptx::cluster_sync();
+  }
   ptx::tc_fence_after_sync();
   if (warp == kMmaWarp) {
     if constexpr (P2)

@@ -24,8 +24,8 @@ constexpr int kSfAtomBytes = 512;          // 128 rows x 4 scales
 constexpr int kSfSlabBytes = 4 * kSfAtomBytes;  // one 128-row block, one k-tile
 
 // Warp roles: kProducerWarps TMA producers, one MMA warp, four epilogue warps
-// (one per 32-lane tensor-memory sub-partition).
-constexpr int kProducerWarps = 2;  // warp 0: A + SFA, warp 1: B + SFB
+// (one per 32-lane tensor-memory sub-partition): 8 warps, two warpgroups.
+constexpr int kProducerWarps = 3;  // warp 0: A + SFA, warp 1: B, warp 2: SFB
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kFirstEpiWarp = kProducerWarps + 1;
 constexpr int kEpiWarps = 4;

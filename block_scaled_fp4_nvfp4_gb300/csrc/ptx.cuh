@@ -332,6 +332,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Counts `bytes` of the current phase's transactions as done without any
+// data: for copies a barrier was armed for but that were never issued.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// 32-bit load / store of shared memory of any CTA of the cluster
+// (shared::cluster address from mapa_shared).
+__device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Bulk copy from this CTA's shared memory into the shared memory of a CTA of
 // the cluster; the destination CTA's mbarrier (shared::cluster address)
 // counts the bytes.  Addresses 16-byte aligned, size a multiple of 16.
