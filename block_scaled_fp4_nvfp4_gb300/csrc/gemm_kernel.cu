@@ -55,6 +55,7 @@ struct SmemCtl {
   uint64_t red_go;    // cluster reduction: every CTA of the cluster may now be written
   uint64_t red_staged;  // cluster reduction: every epilogue warp's staging slots written
   uint64_t red_full;    // cluster reduction: every peer's slice of this CTA's columns landed
+  uint64_t part_full;   // pair stream-K: the other segment's partial landed in the ring
   uint32_t tmem_base;
   volatile int abort;
   int last_flag;
@@ -69,6 +70,8 @@ struct SmemCtl {
   uint32_t arm_bytes[kMaxStages];
   int red_armed;
   uint32_t red_sent;
+  uint32_t part_armed;   // bytes part_full was armed with
+  uint32_t part_issued;  // bytes of partial copies issued
   uint32_t peer_abort[4];  // abort flags the cluster's CTAs published here (index = rank)
 };
 
@@ -200,6 +203,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::mbar_init(ptx::smem_addr(&ctl.red_go), CL);                 // one arrival per CTA of the cluster
     ptx::mbar_init(ptx::smem_addr(&ctl.red_staged), kEpiWarps);
     ptx::mbar_init(ptx::smem_addr(&ctl.red_full), 1);  // armed with the peers' bytes
+    ptx::mbar_init(ptx::smem_addr(&ctl.part_full), 1);
     ctl.abort = 0;
     ctl.last_flag = 0;
     for (int s = 0; s < kMaxStages; ++s) {
@@ -212,6 +216,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     }
     ctl.red_armed = 0;
     ctl.red_sent = 0;
+    ctl.part_armed = 0;
+    ctl.part_issued = 0;
     for (int r = 0; r < 4; ++r) ctl.peer_abort[r] = 0;
     ptx::fence_mbar_init();
   }
@@ -318,6 +324,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         W.drain(bar, parity);
       }
     }
+    if (ctl.part_armed) {
+      const uint32_t bar = ptx::smem_addr(&ctl.part_full);
+      if (!ptx::mbar_try_wait(bar, 0)) {
+        if (ctl.part_armed > ctl.part_issued) ptx::mbar_complete_tx(bar, ctl.part_armed - ctl.part_issued);
+        W.drain(bar, 0);
+      }
+    }
     if constexpr (kRed) {
       constexpr uint32_t kSlotBytes = BN / CL * kBM * 4;
       uint32_t got = 0;
@@ -359,7 +372,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     WorkCursor cur;
     work_begin(p.sched, unit, units, cur, wrank);
     Work x;
+    bool any_item = false;
     while (ok && work_next(p.sched, unit, units, cur, x)) {
+      any_item = true;
       const CUtensorMap* mapA = &p.tmA[x.g];
       const CUtensorMap* mapB = &p.tmB[x.g];
       const uint64_t polA = p.a_streams[x.g] ? pol_stream : pol_keep;
@@ -466,6 +481,57 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
+        }
+      }
+    }
+    // Stream-K finisher of a cluster plan (this CTA's last item is segment 0
+    // of a split tile): warp 0 waits for the other segment's ready flags and
+    // copies its fp32 partial (128 x BN, the workspace layout) into the ring,
+    // piece by piece into the stages as the last MMAs release them, counted
+    // on part_full.  The epilogue then reads it from shared memory instead of
+    // waiting for L2 after its accumulator is complete.
+    if constexpr (CL == 2 && !kRed) {
+      if (warp == 0 && ok && any_item && x.nseg == 2 && x.seg == 0 && p.sched.sk_fixup) {
+        const long long slot = x.tile - p.sched.dp_tiles;
+        const char* src = reinterpret_cast<const char*>(p.workspace + slot * (BN * kBM));
+        const int* flags = p.counters + slot * kEpiWarps;
+        bool ready = true;
+        if (lane == 0) {
+          const uint64_t t0 = ptx::globaltimer();
+          for (int f = 0; f < kEpiWarps && ready; ++f) {
+            for (uint32_t i = 0; ptx::ld_acquire_gpu(flags + f) == 0; ++i) {
+              if ((i & 7u) != 0) continue;
+              if (ctl.abort) {
+                ready = false;
+                break;
+              }
+              if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                ctl.abort = 1;
+                atomicCAS(p.status, 0, kStatusTimeoutProducer);
+                ready = false;
+                break;
+              }
+            }
+          }
+        }
+        if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0)) {
+          ptx::fence_proxy_async_global();  // the copies read what the flags published
+          constexpr uint32_t kPartBytes = BN * kBM * 4;
+          const uint32_t pbar = ptx::smem_addr(&ctl.part_full);
+          ctl.part_armed = kPartBytes;
+          ptx::mbar_arrive_expect_tx_elect(pbar, kPartBytes);
+          for (uint32_t off = 0; off < kPartBytes;) {
+            if (!warp_wait(W, empty_bar(stage), phase ^ 1u, kStatusTimeoutProducer)) break;
+            const uint32_t n = kPartBytes - off < static_cast<uint32_t>(Cfg::kStageBytes) ? kPartBytes - off
+                                                                                         : Cfg::kStageBytes;
+            ptx::bulk_load_elect(smem_base + stage * Cfg::kStageBytes, src + off, n, pbar, pol_stream);
+            ctl.part_issued = off + n;
+            off += n;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
         }
       }
     }
@@ -628,7 +694,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     WorkCursor cur;
     work_begin(p.sched, unit, units, cur, wrank);
     Work x;
+    [[maybe_unused]] uint32_t kt_seen = 0;  // k-tiles of this CTA's work list so far (current item included)
     while (work_next(p.sched, unit, units, cur, x)) {
+      kt_seen += static_cast<uint32_t>(x.kt1 - x.kt0);
       // This CTA's last work item?  Once its accumulator is complete every
       // MMA of the CTA (and of its cluster peer's shared tiles) has read its
       // stage, and no copy will land in the ring again.
@@ -696,6 +764,101 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
             for (int c = 0; c < BN / 32; ++c) store_box(x, 32 * c, &h[16 * c]);
           }
         }
+        continue;
+      }
+
+      if constexpr (CL == 2 && !kRed) {
+        // Stream-K tile of a CTA pair (the schedule's sk_fixup): exactly two
+        // segments, each CTA handling its own 128 rows.  Segment 1 -- the
+        // tile's last k-tiles, its cluster's first stream-K item -- stores its
+        // fp32 partial ([BN/4][128 rows][4], 16 bytes of a row per thread) and
+        // sets one ready flag per epilogue warp.  Segment 0 -- the first
+        // k-tiles, its cluster's last item -- waits for the flag of its warp's
+        // rows, adds the partial to its accumulator (two addends, so the sum
+        // does not depend on which segment finished first) and stores the
+        // tile, staged in the idle ring.
+        if (x.nseg != 2 || !p.sched.sk_fixup) {
+          if (lane == 0) {
+            ctl.abort = 1;
+            atomicCAS(p.status, 0, kStatusBadClusterPlan);
+          }
+          release_acc();
+          break;
+        }
+        const long long slot = x.tile - p.sched.dp_tiles;
+        float4* ws = reinterpret_cast<float4*>(p.workspace) + slot * (BN / 4 * kBM) + row;
+        int* flag = p.counters + slot * kEpiWarps + ew;
+        if (x.seg != 0) {
+#pragma unroll 1
+          for (int q = 0; q < BN / 64; ++q) {
+            float v[64];
+            load_chunk(t_row + 64 * q, v);
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4)
+              __stcg(ws + (16 * q + c4) * kBM, make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]));
+          }
+          release_acc();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) ptx::st_release_gpu(flag, 1);
+          continue;
+        }
+        // Segment 0: the producer copied the partial into the ring, piece j
+        // into the stage after this CTA's last k-tile plus j (kt_seen counts
+        // every k-tile of this CTA's work list).  Each 32-column box is summed,
+        // staged in ring space the partial does not use (the stages after the
+        // pieces, then the tail of the last piece's stage; the warp's own
+        // buffer if neither has room) and stored at once.
+        if (!warp_wait(W, ptx::smem_addr(&ctl.part_full), 0, kStatusTimeoutEpilogue)) {
+          release_acc();
+          break;
+        }
+        {
+          constexpr uint32_t kPartBytes = BN * kBM * 4;
+          constexpr uint32_t kPieces = (kPartBytes + Cfg::kStageBytes - 1) / Cfg::kStageBytes;
+          static_assert(kPieces <= static_cast<uint32_t>(kStages), "partial larger than the ring");
+          constexpr uint32_t kLastPiece = kPartBytes - (kPieces - 1) * Cfg::kStageBytes;
+          constexpr uint32_t kBoxesPerStage = Cfg::kStageBytes / Cfg::kEpiBufBytes;
+          constexpr uint32_t kFreeBoxes = (kStages - kPieces) * kBoxesPerStage;
+          constexpr uint32_t kTailOff = (kLastPiece + Cfg::kEpiBufBytes - 1) / Cfg::kEpiBufBytes * Cfg::kEpiBufBytes;
+          constexpr uint32_t kTailBoxes = (Cfg::kStageBytes - kTailOff) / Cfg::kEpiBufBytes;
+#pragma unroll 1
+          for (int q = 0; q < BN / 32; ++q) {
+            uint32_t r[32];
+            ptx::tmem_load_32cols(t_row + 32 * q, r);
+            ptx::tmem_load_wait();
+            ptx::reg_fence32(r);
+            uint32_t hq[16];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const uint32_t o = ((8 * q + c4) * kBM + row) * 16;
+              const float4 t = ld_shared_v4(smem_base + ((kt_seen + o / Cfg::kStageBytes) % kStages) * Cfg::kStageBytes +
+                                            o % Cfg::kStageBytes);
+              hq[2 * c4] = pack_half2(__uint_as_float(r[4 * c4]) + t.x, __uint_as_float(r[4 * c4 + 1]) + t.y);
+              hq[2 * c4 + 1] = pack_half2(__uint_as_float(r[4 * c4 + 2]) + t.z, __uint_as_float(r[4 * c4 + 3]) + t.w);
+            }
+            if (!rows_live) continue;
+            const uint32_t b = ew * (BN / 32) + q;  // box index in the CTA
+            if (b < kFreeBoxes) {
+              stage_and_store(x, 32 * q, hq,
+                              smem_base + ((kt_seen + kPieces + b / kBoxesPerStage) % kStages) * Cfg::kStageBytes +
+                                  (b % kBoxesPerStage) * Cfg::kEpiBufBytes);
+            } else if (b - kFreeBoxes < kTailBoxes) {
+              stage_and_store(x, 32 * q, hq,
+                              smem_base + ((kt_seen + kPieces - 1) % kStages) * Cfg::kStageBytes + kTailOff +
+                                  (b - kFreeBoxes) * Cfg::kEpiBufBytes);
+            } else {
+              store_box(x, 32 * q, hq);
+            }
+          }
+        }
+        release_acc();
+        // partial consumed: ready for the next launch; drop its L2 lines
+        if (lane == 0) *flag = 0;
+        const char* base = reinterpret_cast<const char*>(reinterpret_cast<const float4*>(p.workspace) +
+                                                         slot * (BN / 4 * kBM) + sub * 32);
+        for (int line = lane; line < (BN / 4) * 4; line += 32)
+          ptx::discard_l2(base + static_cast<size_t>(line >> 2) * (kBM * 16) + (line & 3) * 128);
         continue;
       }
 

@@ -91,7 +91,7 @@ struct TileCfg {
   static constexpr int kEpiBoxCols = 32;
   static constexpr int kEpiBufBytes = 32 * kEpiBoxCols * 2;     // 2 KB
   static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
-  static constexpr int kSmemBudget = 227 * 1024 - 512;           // minus static shared memory
+  static constexpr int kSmemBudget = 227 * 1024 - 1024;          // minus static shared memory
   static constexpr int kStages = (kSmemBudget - kEpiBytes - 1024) / kStageBytes;
   static constexpr int kDynSmem = kStages * kStageBytes + kEpiBytes + 1024;  // +1024 alignment slack
   // Tensor memory: accumulators first, then a ring of scale slots.

@@ -321,12 +321,16 @@ int choose_cluster(const Schedule& s, int sms, bool allow, int bn) {
 // 26.3 us as pairs vs 29.7 us with B multicast).  NVFP4_PAIR = 0 | 1 overrides.
 constexpr int kPairMinKtiles = 4;
 
-// Padded 2-SM pairs for groups with odd m-tile counts: 0 off, 1 by the rule
-// below, 2 whenever valid (NVFP4_PAD_PAIRS overrides; 2 is for tests).  Off
-// by default: on the eight-group MoE workload (27 m-tiles padded to 30, 240
-// pair tiles for 76 pairs) it measured 47.0 vs 45.4 us, the fourth round of
-// tiles on some pairs outweighing the smaller per-SM intake.
-constexpr int kPadPairsMaxPct = 115;
+// Padded 2-SM pairs for groups with odd m-tile counts: 0 off (default), 1 by
+// the rule below, 2 whenever valid (NVFP4_PAD_PAIRS overrides; 2 is for
+// tests).  The rule compares what the busiest SM has to take in: a pair tile
+// k-tile brings 38 KB into each SM (A, half of B, scales) against 54 KB for a
+// 128 x 256 k-tile of one CTA, and the steady state of both is bound by that
+// intake (traced on GB300: 0.38 vs 0.47 us per k-tile).  Off by default: on
+// the eight-group MoE workload (27 m-tiles padded to 30, 240 pair tiles for 76
+// pairs, a fourth round of tiles on some) the padded pairs measured the same
+// as single CTAs (46.45 vs 46.45 us, interleaved A/B on one GB300).
+constexpr int kPadPairsMarginPct = 95;
 int pad_pairs_mode() {
   if (const char* env = getenv("NVFP4_PAD_PAIRS")) {
     const int v = atoi(env);
@@ -352,6 +356,122 @@ bool choose_pair(const Schedule& s, int cluster, int bn) {
 bool red_allowed() {
   if (const char* env = getenv("NVFP4_SKRED")) return atoi(env) != 0;
   return true;
+}
+
+// Stream-K tail for plans of CTA pairs (B multicast or 2-SM MMAs): whole
+// pair tiles are dealt round-robin to the U clusters, which leaves the busiest
+// cluster with more k-tiles than the average when the tiles do not fill whole
+// waves or differ in length (groups with different K).  The trailing part of
+// the pair tiles (in schedule order) is then shared out as stream-K: each
+// cluster gets an equal contiguous run of their k-tiles.  Only splits whose
+// run covers at least the longest such tile are considered, so a tile has at
+// most two segments and the reduction is one partial per split tile (written
+// by the cluster that runs the tile's last k-tiles first, added by the one
+// that runs its first k-tiles last).  NVFP4_PAIR_SK = 1 takes the split
+// minimising the busiest cluster's k-tiles plus kPairSkFixupKtiles for the
+// reduction, 2 forces the smallest valid tail (tests).  Off by default:
+// measured on GB300 (interleaved A/B, one box) the reduction costs about as
+// much SM intake as the balance saves -- the finisher takes in the 128 KB
+// partial (~3.4 k-tiles of intake) and the writer holds its accumulator while
+// it writes one -- 8192^3 166.9 vs 166.9 us, the eight-group MoE workload on
+// padded pairs 52.0 vs 46.5 us.
+constexpr int kPairSkFixupKtiles = 4;
+
+int pair_sk_mode() {
+  if (const char* env = getenv("NVFP4_PAIR_SK")) {
+    const int v = atoi(env);
+    if (v >= 0 && v <= 2) return v;
+  }
+  return 0;
+}
+
+long long plan_cluster_sk(Plan* pl, int units) {
+  Schedule& s = pl->sched;
+  const int C = 2;
+  // back to whole tiles only
+  s.dp_tiles = s.total_tiles;
+  s.sk_iters = 0;
+  s.sk_max_segs = 1;
+  s.sk_fixup = 0;
+  for (int g = 0; g < s.num_groups; ++g) {
+    s.sk_tile_first[g] = s.total_tiles;
+    s.sk_iter_start[g] = 0;
+  }
+  s.sk_iter_start[s.num_groups] = 0;
+  pl->counters = 0;
+  pl->workspace_bytes = 0;
+  const int mode = pair_sk_mode();
+  const int P = s.total_tiles / C;  // pair tiles
+  if (units < 1) return 0;
+  std::vector<int> kt(P);
+  for (int g = 0; g < s.num_groups; ++g)
+    for (int i = s.tile_start[g] / C; i < s.tile_start[g + 1] / C; ++i) kt[i] = s.ktiles[g];
+  // k-tiles of the busiest cluster when pair tiles [0, d) run whole and the rest as stream-K
+  auto cost = [&](int d, long long* sk_out, int* maxkt_out) {
+    std::vector<long long> load(units, 0);
+    for (int i = 0; i < d; ++i) load[i % units] += kt[i];
+    long long dp_max = 0;
+    for (long long v : load) dp_max = v > dp_max ? v : dp_max;
+    long long sk = 0;
+    int maxkt = 0;
+    for (int i = d; i < P; ++i) {
+      sk += kt[i];
+      maxkt = kt[i] > maxkt ? kt[i] : maxkt;
+    }
+    *sk_out = sk;
+    *maxkt_out = maxkt;
+    return dp_max + (sk + units - 1) / units + (sk > 0 ? kPairSkFixupKtiles : 0);
+  };
+  long long sk = 0;
+  int maxkt = 0;
+  int best_d = P;
+  long long best = cost(P, &sk, &maxkt);
+  if (mode == 0 || units < 2) return best;
+  // tails of the last partial wave plus w whole waves, w = 0, 1, ...
+  for (int d = P - P % units; d >= 0; d -= units) {
+    if (d == P) continue;  // no tail: the baseline above
+    const long long c = cost(d, &sk, &maxkt);
+    if (sk < static_cast<long long>(maxkt) * units) continue;  // a tile would get three segments
+    if (mode == 2) {  // forced: the smallest valid tail
+      best_d = d;
+      break;
+    }
+    if (c < best) {
+      best = c;
+      best_d = d;
+    }
+  }
+  if (best_d == P) return best;
+  s.dp_tiles = best_d * C;
+  long long T = 0;
+  for (int g = 0; g < s.num_groups; ++g) {
+    const long long first = s.dp_tiles > s.tile_start[g] ? s.dp_tiles : s.tile_start[g];
+    const long long count = s.tile_start[g + 1] > first ? s.tile_start[g + 1] - first : 0;
+    s.sk_tile_first[g] = static_cast<int>(first);
+    s.sk_iter_start[g] = T;
+    T += count / C * s.ktiles[g];
+  }
+  s.sk_iter_start[s.num_groups] = T;
+  s.sk_iters = T;
+  s.sk_max_segs = 2;
+  s.sk_fixup = 1;
+  // one fp32 partial of 128 x BN per stream-K CTA tile, and one ready flag
+  // per epilogue warp of each
+  const long long sk_tiles = s.total_tiles - s.dp_tiles;
+  pl->counters = static_cast<int>(sk_tiles * kEpiWarps);
+  pl->workspace_bytes = static_cast<size_t>(sk_tiles) * kBM * pl->bn * sizeof(float);
+  return best;
+}
+
+// k-tiles of the busiest CTA of a data-parallel single-CTA plan (whole tiles
+// dealt round-robin to `grid` CTAs).
+long long busiest_cta_ktiles(const Schedule& s, int grid) {
+  std::vector<long long> load(grid, 0);
+  for (int g = 0; g < s.num_groups; ++g)
+    for (int t = s.tile_start[g]; t < s.tile_start[g + 1]; ++t) load[t % grid] += s.ktiles[g];
+  long long m = 0;
+  for (long long v : load) m = v > m ? v : m;
+  return m;
 }
 
 int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int sms, Plan* pl,
@@ -464,8 +584,9 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     // such group: A and its scales are read through tensor maps, so the
     // padding rows load as zeros, and the epilogue stores no row past M.
     // (B-multicast pairs load the A scales with plain bulk copies and
-    // cannot be padded.)  Taken when the padding adds at most
-    // kPadPairsMaxPct percent of tiles and the pairs fill two waves.
+    // cannot be padded.)  Taken when the busiest pair's estimated intake
+    // (with its stream-K tail) is below kPadPairsMarginPct percent of the
+    // busiest single CTA's.
     long long padded = 0;
     for (int g = 0; g < G; ++g) padded += static_cast<long long>((pl->tiles_m[g] + 1) & ~1) * pl->tiles_n[g] * L[g];
     Schedule ps = s;
@@ -479,17 +600,21 @@ int make_plan(int G, const int* M, const int* N, const int* K, const int* L, int
     ps.total_tiles = ps.dp_tiles = static_cast<int>(t);
     for (int g = 0; g < G; ++g) ps.sk_tile_first[g] = ps.total_tiles;
     ps.cluster = 2;
-    const bool worth = pad_pairs_mode() == 2 || (padded * 100 <= tiles * kPadPairsMaxPct && padded >= 2 * sms);
-    if (padded > tiles && worth && choose_pair(ps, 2, pl->bn)) {
-      s = ps;
-      for (int g = 0; g < G; ++g) pl->tiles_m[g] = ps.tiles_m[g];
-      pl->cluster = 2;
-      pl->pair = true;
+    if (sms >= 2 && padded > tiles && (padded >= sms || pad_pairs_mode() == 2) && choose_pair(ps, 2, pl->bn)) {
+      Plan pp = *pl;
+      pp.sched = ps;
+      for (int g = 0; g < G; ++g) pp.tiles_m[g] = ps.tiles_m[g];
+      pp.cluster = 2;
+      pp.pair = true;
       const long long groups = padded / 2;
       const long long per_wave = sms / 2;
-      pl->grid = static_cast<int>((groups < per_wave ? groups : per_wave) * 2);
+      pp.grid = static_cast<int>((groups < per_wave ? groups : per_wave) * 2);
+      const long long pair_intake = plan_cluster_sk(&pp, pp.grid / 2) * TileCfg<256, true>::kStageBytes;
+      const long long single_intake = busiest_cta_ktiles(s, pl->grid) * TileCfg<256>::kStageBytes;
+      if (pad_pairs_mode() == 2 || pair_intake * 100 < single_intake * kPadPairsMarginPct) *pl = pp;
     }
   }
+  if (pl->cluster == 2 && !pl->red) plan_cluster_sk(pl, pl->grid / 2);
   pl->stages = gemm_stages(pl->bn, pl->pair);
   return NVFP4_OK;
 }
@@ -685,8 +810,11 @@ int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B, co
       if ((rc = make_plan(G, M, N, K, L, ds->sms, &pl, /*allow_cluster=*/false)) != NVFP4_OK) return rc;
     } else if (!pl.red && pl.grid / pl.cluster > mc) {
       // persistent grid: no more clusters than can be co-resident (a reduction
-      // cluster runs one tile and waits on no other cluster, so it needs none)
+      // cluster runs one tile and waits on no other cluster, so it needs none;
+      // a stream-K tail does wait on other clusters' partials, so it must be
+      // planned for the clusters that actually run at once)
       pl.grid = mc * pl.cluster;
+      plan_cluster_sk(&pl, pl.grid / 2);
     }
   }
 

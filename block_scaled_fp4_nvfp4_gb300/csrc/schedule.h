@@ -5,9 +5,15 @@
 // contiguous range per CTA).
 //
 // Stream-K: iteration x of the stream-K space belongs to tile x / KT (per
-// group), and CTA c owns iterations [floor(c*T/G), floor((c+1)*T/G)).  A tile
-// covered by several CTAs gets one partial result per covering CTA ("segment"),
-// numbered in k order; the last segment to finish sums them in that order.
+// group), and unit c owns iterations [floor(c*T/G), floor((c+1)*T/G)).  A unit
+// is one CTA, or one cluster of two CTAs running tiles 2q and 2q+1 (the same
+// B columns) over the same k-range.  A tile covered by several units gets one
+// partial result per covering unit ("segment"), numbered in k order; the last
+// segment to finish sums them in that order.  In cluster plans (sk_fixup)
+// every unit covers at least one whole tile's k-tiles, so a tile has at most
+// two segments: segment 1 (the tile's last k-tiles) is the first item of its
+// unit and publishes its partial; segment 0 is the last item of the previous
+// unit, which adds that partial and stores the tile.
 #pragma once
 
 #include <stdint.h>
@@ -34,6 +40,7 @@ struct Schedule {
   long long sk_iters;  // T: total stream-K iterations (0 = no stream-K part)
   int sk_max_segs;  // workspace slots reserved per stream-K tile
   int cluster;      // CTAs per cluster (1, or 2: the pair runs tiles 2q, 2q+1, sharing B)
+  int sk_fixup;     // 1: stream-K tiles of a cluster plan, at most two segments (see above)
 };
 
 struct Work {
@@ -55,8 +62,9 @@ NVFP4_HD int sk_owner(long long y, long long T, int G) {
 }
 
 // `cta` / `grid` count clusters; `rank` is the CTA's rank inside its cluster.
-// With clusters of 2 the plan is data-parallel only and every group has an
-// even number of m-tiles, so tiles 2q and 2q+1 (m fastest) share g, l, tn.
+// With clusters of 2 every group has an even number of m-tiles and the
+// stream-K part starts at an even tile of each group, so tiles 2q and 2q+1
+// (m fastest) share g, l, tn.
 NVFP4_HD void work_begin(const Schedule& s, int cta, int grid, WorkCursor& cur, int rank = 0) {
   cur.dp_next = cta;
   cur.rank = rank;
@@ -100,7 +108,7 @@ NVFP4_HD bool work_next(const Schedule& s, int cta, int grid, WorkCursor& cur, W
   const long long t_begin = cur.x - k0;  // first iteration of this tile
   const long long t_end = t_begin + KT;
   const long long end = cur.hi < t_end ? cur.hi : t_end;
-  tile_coords(s, s.sk_tile_first[g] + static_cast<int>(local / KT), w);
+  tile_coords(s, s.sk_tile_first[g] + static_cast<int>(local / KT) * s.cluster + cur.rank, w);
   w.kt0 = static_cast<int>(k0);
   w.kt1 = static_cast<int>(end - t_begin);
   const int first = sk_owner(t_begin, s.sk_iters, grid);

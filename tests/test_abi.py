@@ -58,8 +58,9 @@ def test_plan_single_tile_and_full_machine(lib):
     assert p["bn"] == 128 and p["tiles"] == 1 and p["grid"] == 1
     assert p["stages"] >= 4 and p["sk_max_segs"] == 1
     p = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
-    # 128 x 256 tiles: 2048 of them, all data-parallel
-    assert p["bn"] == 256 and p["tiles"] == 2048 and p["dp_tiles"] == 2048 and p["grid"] == 152
+    # 128 x 256 tiles: 2048 of them as 2-SM pairs, the last wave and a half stream-K
+    assert p["bn"] == 256 and p["tiles"] == 2048 and p["grid"] == 152
+    assert p["dp_tiles"] + p["sk_tiles"] == 2048
 
 
 def test_plan_stream_k_for_skinny_problem(lib):
@@ -71,13 +72,24 @@ def test_plan_stream_k_for_skinny_problem(lib):
     assert p["grid"] == 16 and p["sk_max_segs"] == 4         # capped: >= 4 k-tiles per CTA
 
 
-def test_plan_data_parallel_from_one_wave(lib):
+def test_plan_data_parallel_from_one_wave(lib, monkeypatch):
     Ms = [384, 64, 1024, 256, 192, 512, 128, 768]
     p = binding.nvfp4_gemm_plan(Ms, [4096] * 8, [7168] * 8, [1] * 8, 152)
     tiles = sum(-(-m // 128) for m in Ms) * 16
     assert p["bn"] == 256 and p["tiles"] == tiles == 432 and p["dp_tiles"] == 432 and p["sk_tiles"] == 0
+    # by the intake rule with a stream-K tail: padded to 2-SM pairs (30
+    # m-tiles instead of 27), two whole waves, the rest stream-K
+    monkeypatch.setenv("NVFP4_PAD_PAIRS", "1")
+    monkeypatch.setenv("NVFP4_PAIR_SK", "1")
+    p = binding.nvfp4_gemm_plan(Ms, [4096] * 8, [7168] * 8, [1] * 8, 152)
+    padded = sum((-(-m // 128) + 1) // 2 * 2 for m in Ms) * 16
+    assert p["bn"] == 256 and p["pair"] == 1 and p["tiles"] == padded == 480
+    assert p["dp_tiles"] == 2 * 2 * 76 and p["sk_tiles"] == 480 - 304
+    _check_pair_sk(Ms, [4096] * 8, [7168] * 8, [1] * 8, 152)
+    monkeypatch.delenv("NVFP4_PAD_PAIRS")
+    monkeypatch.delenv("NVFP4_PAIR_SK")
     p = binding.nvfp4_gemm_plan([1024, 2048], [4096, 7168], [7168, 2048], [1, 1], 152)
-    assert p["bn"] == 256 and p["tiles"] == 8 * 16 + 16 * 28 == p["dp_tiles"]
+    assert p["bn"] == 256 and p["tiles"] == 8 * 16 + 16 * 28 == p["dp_tiles"] + p["sk_tiles"]
 
 
 SCHED_CASES = [
@@ -91,8 +103,20 @@ SCHED_CASES = [
 ]
 
 
+def _tiles_m(M, N, L, plan):
+    """m-tiles per group as planned: 2-SM pair plans over groups with an odd
+    number of m-tiles pad each such group by one m-tile."""
+    tm = [-(-m // 128) for m in M]
+    plain = sum(t * -(-n // plan["bn"]) * l for t, n, l in zip(tm, N, L))
+    if plan["tiles"] != plain:
+        tm = [(t + 1) // 2 * 2 for t in tm]
+        assert plan["pair"] == 1 and plan["tiles"] == sum(t * -(-n // plan["bn"]) * l for t, n, l in zip(tm, N, L))
+    return tm
+
+
 def _check_schedule(M, N, K, L, sms):
     plan = binding.nvfp4_gemm_plan(M, N, K, L, sms)
+    tms = _tiles_m(M, N, L, plan)
     cover = {}
     segs = {}
     sk_lengths = []
@@ -101,7 +125,7 @@ def _check_schedule(M, N, K, L, sms):
         sk = 0
         for w in items:
             g = w["g"]
-            tiles_m, tiles_n, kt = -(-M[g] // 128), -(-N[g] // plan["bn"]), K[g] // 256
+            tiles_m, tiles_n, kt = tms[g], -(-N[g] // plan["bn"]), K[g] // 256
             assert 0 <= w["tm"] < tiles_m and 0 <= w["tn"] < tiles_n and 0 <= w["l"] < L[g]
             assert 0 <= w["kt0"] < w["kt1"] <= kt
             key = (g, w["l"], w["tm"], w["tn"])
@@ -113,7 +137,7 @@ def _check_schedule(M, N, K, L, sms):
                 sk += w["kt1"] - w["kt0"]
         sk_lengths.append(sk)
     # every k-tile of every tile exactly once
-    total = sum(-(-M[g] // 128) * -(-N[g] // plan["bn"]) * L[g] * (K[g] // 256) for g in range(len(M)))
+    total = sum(tms[g] * -(-N[g] // plan["bn"]) * L[g] * (K[g] // 256) for g in range(len(M)))
     assert len(cover) == total
     # segments of a tile: indices 0..n-1, consistent count, in k order, same coordinates
     assert len(segs) == plan["tiles"]
@@ -303,3 +327,76 @@ def test_cluster_reduction_planned_for_one_segment_per_cta(lib, monkeypatch):
     monkeypatch.setenv("NVFP4_SKRED", "1")
     monkeypatch.setenv("NVFP4_SCHEDULE", "sk")   # uneven ranges: workspace path
     assert binding.nvfp4_gemm_plan([128], [7168], [16384], [1], 152)["cluster_reduce"] == 0
+
+
+# ------------------------------------------------------------------ stream-K tails of CTA-pair plans
+def _check_pair_sk(M, N, K, L, sms):
+    """A cluster plan with a stream-K tail: every k-tile once (checked by
+    _check_schedule), at most two segments per tile, both CTAs of a cluster
+    on the same k-range of tiles 2q and 2q+1, and the order the reduction
+    relies on: segment 1 of a split tile is the first stream-K item of its
+    cluster, segment 0 the last item of its cluster."""
+    _check_schedule(M, N, K, L, sms)
+    plan = binding.nvfp4_gemm_plan(M, N, K, L, sms)
+    assert plan["cluster"] == 2 and plan["sk_max_segs"] <= 2
+    items = [binding.nvfp4_gemm_debug_schedule(M, N, K, L, sms, c) for c in range(plan["grid"])]
+    for c in range(0, plan["grid"], 2):
+        a, b = items[c], items[c + 1]
+        assert len(a) == len(b)
+        for x, y in zip(a, b):
+            assert (x["g"], x["l"], x["tn"], x["kt0"], x["kt1"], x["seg"], x["nseg"]) == \
+                   (y["g"], y["l"], y["tn"], y["kt0"], y["kt1"], y["seg"], y["nseg"])
+            assert y["tm"] == x["tm"] + 1 and x["tm"] % 2 == 0
+    for cta, lst in enumerate(items):
+        sk = [w for w in lst if w["tile"] >= plan["dp_tiles"]]
+        for i, w in enumerate(sk):
+            assert w["nseg"] in (1, 2)
+            if w["nseg"] == 2:
+                assert (w["seg"] == 1 and i == 0) or (w["seg"] == 0 and i == len(sk) - 1 and w is lst[-1]), (cta, w)
+    return plan
+
+
+def test_dense_pair_plan_gets_a_stream_k_tail(lib, monkeypatch):
+    """8192^3 as 2-SM pairs on 152 SMs: 1024 pair tiles over 76 clusters leave a
+    partial 14th wave; by the rule (NVFP4_PAIR_SK=1) one wave plus the
+    remainder (112 pair tiles) run as stream-K, 47.2 k-tiles per cluster
+    instead of whole 32-k-tile tiles."""
+    monkeypatch.setenv("NVFP4_PAIR_SK", "1")
+    plan = _check_pair_sk([8192], [8192], [8192], [1], 152)
+    assert plan["pair"] == 1 and plan["sk_tiles"] == 2 * 112 and plan["dp_tiles"] == 2 * 912
+
+
+def test_grouped_pair_plan_never_worse_than_whole_tiles(lib, monkeypatch):
+    """Two groups whose tiles have 28 and 8 k-tiles: whole tiles dealt
+    round-robin leave the busiest cluster 52 k-tiles (47.2 on average); a
+    stream-K tail is taken only where its estimate (busiest cluster plus the
+    reduction) is lower, so the busiest cluster never gets more."""
+    monkeypatch.setenv("NVFP4_PAIR_SK", "1")
+    M, N, K, L = [1024, 2048], [4096, 7168], [7168, 2048], [1, 1]
+    plan = _check_pair_sk(M, N, K, L, 152)
+    per = []
+    for c in range(0, plan["grid"], 2):
+        per.append(sum(w["kt1"] - w["kt0"] for w in binding.nvfp4_gemm_debug_schedule(M, N, K, L, 152, c)))
+    assert max(per) <= 52 and sum(per) == 3584
+
+
+@pytest.mark.parametrize("shape", [([512], [1024], [4096], [1]), ([256, 768], [512, 264], [2048, 1024], [1, 2]),
+                                   ([1024], [2048], [1536], [2])])
+@pytest.mark.parametrize("sms", [16, 36, 152])
+def test_forced_pair_stream_k_tails(lib, shape, sms, monkeypatch):
+    for k, v in {"NVFP4_BN": "256", "NVFP4_SCHEDULE": "dp", "NVFP4_CLUSTER": "2", "NVFP4_PAIR_SK": "2"}.items():
+        monkeypatch.setenv(k, v)
+    for pair in ("1", "0"):
+        monkeypatch.setenv("NVFP4_PAIR", pair)
+        plan = binding.nvfp4_gemm_plan(*shape, sms)
+        if plan["cluster"] != 2:
+            continue
+        _check_pair_sk(*shape, sms)
+
+
+def test_pair_stream_k_is_off_by_default(lib, monkeypatch):
+    monkeypatch.delenv("NVFP4_PAIR_SK", raising=False)
+    plan = binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)
+    assert plan["pair"] == 1 and plan["sk_tiles"] == 0
+    monkeypatch.setenv("NVFP4_PAIR_SK", "1")
+    assert binding.nvfp4_gemm_plan([8192], [8192], [8192], [1], 152)["sk_tiles"] > 0
