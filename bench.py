@@ -406,7 +406,6 @@ def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
         l2_note = "rotating %d input sets, %.0f MB > 3 x L2 (%.0f MB)" % (sets, sets * wl.bytes / 1e6, l2 / 1e6)
     host0, dev_sets = device_inputs(binding, wl, sets, dev)
     elapsed_ms, tw0, tw1 = time_launches(binding, dev_sets, args.steps, args.warmup, stream, flush)
-    del flush
     launch = binding.nvfp4_gemm_last_launch()
     launch_s = elapsed_ms / args.steps * 1e-3
     bound, t_hbm, t_fp4, hbm, fp4 = roofline_terms(wl, peaks)
@@ -414,7 +413,9 @@ def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
         achieved, peak, unit = wl.bytes / launch_s / 1e9, hbm, "GB/s"
     else:
         achieved, peak, unit = wl.flops / launch_s / 1e12, fp4, "TFLOP/s"
-    copy_ref = size_matched_copy(wl.bytes, dev, stream, l2) if bound == "hbm" else None
+    # a same-size copy is only meaningful where the inputs rotate through more
+    # than L2 (not for the launch-latency-bound single tile)
+    copy_ref = size_matched_copy(wl.bytes, dev, stream, l2) if bound == "hbm" and flush is None else None
     res = {
         "workload": wl.name, "shapes_MNKL": wl.shapes, "steps": args.steps, "warmup": args.warmup,
         "us_per_launch": launch_s * 1e6, "tflops": wl.flops / launch_s / 1e12,
@@ -431,6 +432,7 @@ def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
         "roofline_fraction_min_time": max(t_hbm, t_fp4) / launch_s,
         "_wall": (tw0, tw1),
     }
+    del flush
     if args.check:
         res["check"] = check_sampled(host0, dev_sets[0])
     return res, host0, dev_sets
@@ -480,6 +482,41 @@ def quantize_leg(binding, dev, stream, hbm):
     ach = nbytes / (ms * 1e-3) / 1e9
     return {"shape_LxRxK": [ql, qr, qk], "input": "bf16", "us": ms * 1e3, "algorithmic_bytes": nbytes,
             "achieved": ach, "unit": "GB/s", "peak": hbm, "frac": ach / hbm}
+
+
+def repack_leg(binding, dev, stream, l2, hbm, rows=7168, K=16384, iters=50):
+    """The scale repack alone (a once-per-weight preparation, outside the
+    timed step): row-major [rows, K/16] E4M3 scales -> the atom layout, for
+    the skinny workload's B scales (7168 x 1024 bytes), rotating over buffer
+    pairs larger than L2 together, against a copy of the same bytes."""
+    cols = K // 16
+    nbytes_in = rows * cols
+    nbytes_out = binding.nvfp4_gemm_repacked_scales_bytes(rows, K, 1)
+    per = nbytes_in + nbytes_out
+    sets = max(2, math.ceil(3 * l2 / per) + 1)
+    g = torch.Generator(device=dev).manual_seed(0)
+    src = [torch.randint(0, 127, (rows, cols), dtype=torch.uint8, device=dev, generator=g) for _ in range(sets)]
+    dst = [torch.empty(nbytes_out, dtype=torch.uint8, device=dev) for _ in range(sets)]
+    with torch.cuda.stream(stream):
+        for i in range(sets):
+            binding.nvfp4_gemm_repack_scales(src[i], dst[i], rows, K, 1, stream)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(iters):
+            binding.nvfp4_gemm_repack_scales(src[i % sets], dst[i % sets], rows, K, 1, stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    binding.nvfp4_gemm_check_device_status(stream)
+    us = t0.elapsed_time(t1) / iters * 1e3
+    ach = per / (us * 1e-6) / 1e9
+    del src, dst
+    copy = size_matched_copy(per, dev, stream, l2)
+    return {"rows_x_scale_bytes": [rows, cols], "bytes_read": nbytes_in, "bytes_written": nbytes_out, "us": us,
+            "achieved": ach, "unit": "GB/s", "peak": hbm, "frac": ach / hbm, "size_matched_copy": copy,
+            "frac_of_size_matched_copy": ach / copy["achieved"],
+            "l2": "rotating %d buffer pairs, %.0f MB > 3 x L2" % (sets, sets * per / 1e6)}
 
 
 def e2e_leg(binding, host0, steps, dev, stream, flops):
@@ -602,6 +639,7 @@ def main(argv=None):
     torch.cuda.empty_cache()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     extra["quantize"] = None if args.no_quantize else quantize_leg(binding, dev, stream, hbm)
+    extra["repack"] = None if args.no_repack_step else repack_leg(binding, dev, stream, l2, hbm)
     e2e = e2e_leg(binding, host0, args.e2e_steps, dev, stream, wl.flops)
     sampler.stop()
 
