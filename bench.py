@@ -527,9 +527,9 @@ def e2e_leg(binding, host0, steps, dev, stream, flops):
     h2d = d2h = 0
     for p in host0:
         e = {k: p[k].pin_memory() for k in ("A", "B", "SFA", "SFB")}
-        e["Cout"] = torch.empty((p["L"], p["M"], p["N"]), dtype=torch.float16).pin_memory()
+        e["Cout"] = [torch.empty((p["L"], p["M"], p["N"]), dtype=torch.float16).pin_memory() for _ in range(2)]
         h2d += sum(e[k].numel() * e[k].element_size() for k in ("A", "B", "SFA", "SFB"))
-        d2h += e["Cout"].numel() * 2
+        d2h += e["Cout"][0].numel() * 2
         hp.append(e)
 
     def device_buffers():
@@ -546,33 +546,41 @@ def e2e_leg(binding, host0, steps, dev, stream, flops):
                             C=torch.empty((L, M, N), dtype=torch.float16, device=dev)))
         return out
 
-    # Two device buffer sets: the host->device copies of step i+1 (on their own
-    # stream) overlap the repacks, GEMM and readback of step i; every step still
-    # copies its own inputs and reads back its own result inside the timed region.
+    # Two device buffer sets and three streams: step i+1's host-to-device
+    # copies (copy stream) and step i's device-to-host readback (readback
+    # stream) overlap step i+1's repacks and GEMM (compute stream); every step
+    # still copies its own inputs in and its own result out inside the timed
+    # region, and a set is refilled only after its previous result was read.
     ed_sets = [device_buffers(), device_buffers()]
     copy_stream = torch.cuda.Stream(device=dev)
+    read_stream = torch.cuda.Stream(device=dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
+    computed = [torch.cuda.Event(), torch.cuda.Event()]
     freed = [torch.cuda.Event(), torch.cuda.Event()]
 
     def step(i):
-        ed = ed_sets[i % 2]
+        j = i % 2
+        ed = ed_sets[j]
         with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(freed[i % 2])  # the set's previous step is done with it
+            copy_stream.wait_event(freed[j])  # the set's previous result has been read back
             for e, q in zip(hp, ed):
                 q["A"].copy_(e["A"], non_blocking=True)
                 q["B"].copy_(e["B"], non_blocking=True)
                 q["SFAraw"].copy_(e["SFA"], non_blocking=True)
                 q["SFBraw"].copy_(e["SFB"], non_blocking=True)
-            copied[i % 2].record(copy_stream)
-        stream.wait_event(copied[i % 2])
+            copied[j].record(copy_stream)
+        stream.wait_event(copied[j])
         with torch.cuda.stream(stream):
             for q in ed:
                 binding.nvfp4_gemm_repack_scales(q["SFAraw"], q["SFA"], q["M"], q["K"], q["L"], stream)
                 binding.nvfp4_gemm_repack_scales(q["SFBraw"], q["SFB"], q["N"], q["K"], q["L"], stream)
             launch_grouped(binding, ed, stream)
+            computed[j].record(stream)
+        read_stream.wait_event(computed[j])
+        with torch.cuda.stream(read_stream):
             for e, q in zip(hp, ed):
-                e["Cout"].copy_(q["C"], non_blocking=True)
-            freed[i % 2].record(stream)
+                e["Cout"][j].copy_(q["C"], non_blocking=True)
+            freed[j].record(read_stream)
 
     for i in range(3):
         step(i)
@@ -582,14 +590,17 @@ def e2e_leg(binding, host0, steps, dev, stream, flops):
     copy_stream.wait_event(e0)  # no copy of the timed steps starts before the clock does
     for i in range(steps):
         step(i)
+    stream.wait_event(freed[(steps - 1) % 2])  # the clock stops once the last result is on the host
+    if steps > 1:
+        stream.wait_event(freed[(steps - 2) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     binding.nvfp4_gemm_check_device_status(stream)
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "includes": "H2D of A, B, row-major SFA/SFB; 2 repacks; GEMM; D2H of C; two buffer "
-                        "sets, step i+1's copies overlapping step i"}
+            "includes": "H2D of A, B, row-major SFA/SFB; 2 repacks; GEMM; D2H of C; two buffer sets, "
+                        "step i+1's copies in and step i's readback overlapping step i+1's work"}
 
 
 # ------------------------------------------------------------------ our arm
