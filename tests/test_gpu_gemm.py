@@ -553,3 +553,23 @@ def test_padded_pair_tiles(shapes, monkeypatch):
     for p, (buf, c) in zip(probs, Cs):
         check_canary(buf, p["M"], p["N"], p["L"])
         assert_close_full(c, p)
+
+
+@pytest.mark.parametrize("M,N,K,L", [
+    (128, 256, 65536, 1),    # K = 2^16: 64 stream-K segments per tile, summed through the workspace
+    (1, 8, 65536, 1),        # a single 1 x 8 output row over 64 segments
+    (8, 65528, 256, 1),      # very wide, 8 rows: 256 tiles of 128 x 256, mostly padding rows
+    (4096, 8, 512, 1),       # very tall, 8 columns: N smaller than every tile width
+    (300, 200, 4096, 6),     # six batches, ragged everywhere, clusters of four reducing
+])
+def test_parity_extreme_shapes(M, N, K, L):
+    """Extreme aspect ratios and depths under the default planner, element by
+    element against the oracle."""
+    binding = require_gpu()
+    p = workloads.make_random_problem(M + N + K + L, M, N, K, L)
+    d = to_device(p)
+    buf, C = alloc_c(M, N, L)
+    run_single(d, C)
+    binding.nvfp4_gemm_check_device_status()
+    assert_close_full(C, p)
+    check_canary(buf, M, N, L)
