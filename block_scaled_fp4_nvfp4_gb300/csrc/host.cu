@@ -87,6 +87,11 @@ struct Workspace {
   size_t partial_bytes = 0;
   int* counters = nullptr;
   size_t counter_count = 0;
+  // Buffers replaced by larger ones.  They are never freed: a CUDA graph
+  // captured with an earlier launch names them in its kernel parameters.
+  // Growth at least doubles, so these add up to less than the live buffers.
+  std::vector<void*> retired_partials;
+  std::vector<std::pair<int*, size_t>> retired_counters;
 };
 
 std::mutex g_mu;
@@ -678,15 +683,21 @@ int get_workspace(int dev, cudaStream_t stream, size_t partial_bytes, size_t cou
     if ((e = cudaStreamIsCapturing(stream, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     if (cs != cudaStreamCaptureStatusNone)
       return fail(NVFP4_ERR_INVALID_ARG,
-                  "split-K workspace must grow while the stream is being captured; run the same "
-                  "problem once on this stream before capturing it");
-    // the old buffers may still be in use by work queued on this stream
-    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    cudaFree(w.partials);
-    cudaFree(w.counters);
-    w = Workspace{};
-    const size_t pb = partial_bytes > 0 ? partial_bytes : 16;
-    const size_t cb = (counters > 0 ? counters : 1) * sizeof(int);
+                  "the split-K workspace would have to grow while the stream is being captured; run "
+                  "the same problem once on this stream before capturing it");
+    // The old buffers stay allocated (work queued on this stream, or a graph
+    // captured earlier, may still use them); the new ones at least double.
+    if (w.partials) w.retired_partials.push_back(w.partials);
+    if (w.counters) w.retired_counters.emplace_back(w.counters, w.counter_count);
+    size_t pb = partial_bytes > 0 ? partial_bytes : 16;
+    if (pb < 2 * w.partial_bytes) pb = 2 * w.partial_bytes;
+    size_t cn = counters > 0 ? counters : 1;
+    if (cn < 2 * w.counter_count) cn = 2 * w.counter_count;
+    const size_t cb = cn * sizeof(int);
+    w.partials = nullptr;
+    w.counters = nullptr;
+    w.partial_bytes = 0;
+    w.counter_count = 0;
     if ((e = cudaMalloc(&w.partials, pb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K workspace)");
     if ((e = cudaMalloc(&w.counters, cb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K counters)");
     if ((e = cudaMemsetAsync(w.counters, 0, cb, stream)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
@@ -899,10 +910,15 @@ int nvfp4_gemm_check_device_status(void* stream_) {
     // every workspace of this device before reporting.
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     if ((e = cudaMemset(ds->status, 0, sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
-    for (auto& kv : g_workspaces)
-      if (kv.first.first == dev && kv.second.counters)
+    for (auto& kv : g_workspaces) {
+      if (kv.first.first != dev) continue;
+      if (kv.second.counters)
         if ((e = cudaMemset(kv.second.counters, 0, kv.second.counter_count * sizeof(int))) != cudaSuccess)
           return cuda_fail(e, "cudaMemset(counters)");
+      for (const auto& rc_buf : kv.second.retired_counters)
+        if ((e = cudaMemset(rc_buf.first, 0, rc_buf.second * sizeof(int))) != cudaSuccess)
+          return cuda_fail(e, "cudaMemset(counters)");
+    }
     return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a bounded wait ran out on the device (role code %d)", h);
   }
   return ok();

@@ -8,68 +8,73 @@
 // grouped_kernel TMA producer).  rest_k is padded to whole 256-wide k-tiles;
 // padding is zero.
 //
-// One thread writes eight 16-byte atom rows: row r0 of the eight consecutive
-// atoms ck = 8*j8 .. 8*j8+7 of one 128-row block.  It reads 32 contiguous
-// bytes (eight groups of four scales) from each of rows r0, r0+32, r0+64 and
-// r0+96 -- whole 32-byte sectors when the row pitch K/16 is a multiple of 16
-// -- and for each atom the 32 threads of a warp store 512 contiguous bytes.
+// One CTA transposes a 128-row x 128-column tile of scales (the 32 atoms of
+// one 128-row block and eight k-tiles) through shared memory: it reads the
+// tile row by row (each warp four 128-byte row segments per instruction) and
+// writes the 32 atoms as 16 KB of contiguous output (each warp one 512-byte
+// atom per instruction).  The shared tile has a 33-word row pitch, so both
+// the row-wise stores and the atom-wise reads hit 32 different banks.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace nvfp4 {
 
-constexpr int kAtomsPerThread = 8;
+constexpr int kTileRows = 128;   // one 128-row scale block
+constexpr int kTileCols = 128;   // scale bytes per row: 32 atoms, eight 256-wide k-tiles
+constexpr int kPitchWords = kTileCols / 4 + 1;
+constexpr int kRepackThreads = 256;
 
-__global__ void __launch_bounds__(256) repack_scales_kernel(const uint8_t* __restrict__ sf,
-                                                            uint8_t* __restrict__ out, int rows,
-                                                            int cols, int rest_m, int rest_k,
-                                                            long long work) {
-  const long long q = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (q >= work) return;
-  // q = (((l * rest_m + rm) * groups + j8) * 32 + r0), groups = ceil(rest_k / 8)
-  const int groups = (rest_k + kAtomsPerThread - 1) / kAtomsPerThread;
-  const int r0 = static_cast<int>(q & 31);
-  long long t = q >> 5;
-  const int j8 = static_cast<int>(t % groups);
-  t /= groups;
-  const int rm = static_cast<int>(t % rest_m);
-  const long long l = t / rest_m;
-  const int c0 = j8 * kAtomsPerThread * 4;  // first scale column of atom 8*j8
-  uint32_t w[4][kAtomsPerThread];
-  const bool wide = (cols & 15) == 0 && c0 + kAtomsPerThread * 4 <= cols;
-  const bool aligned_cols = (cols & 3) == 0;
+__global__ void __launch_bounds__(kRepackThreads) repack_scales_kernel(const uint8_t* __restrict__ sf,
+                                                                       uint8_t* __restrict__ out, int rows,
+                                                                       int cols, int rest_m, int rest_k,
+                                                                       int ctiles) {
+  __shared__ uint32_t tile[kTileRows * kPitchWords];
+  // block = (l * rest_m + rm) * ctiles + ct
+  const int ct = static_cast<int>(blockIdx.x % static_cast<unsigned>(ctiles));  // atoms 32*ct .. 32*ct+31
+  const long long lm = blockIdx.x / static_cast<unsigned>(ctiles);
+  const int rm = static_cast<int>(lm % rest_m);                                  // 128-row block
+  const long long l = lm / rest_m;
+  const int t = threadIdx.x;
+  const int c_base = ct * kTileCols;
+  const bool vec = (cols & 15) == 0;         // every row starts 16-byte aligned
+  const bool words = (cols & 3) == 0;        // every row starts 4-byte aligned
+  // load: element i of the 128 x 8 grid of 16-byte chunks, zero past the edges
 #pragma unroll
-  for (int r1 = 0; r1 < 4; ++r1) {
-    const int r = rm * 128 + r1 * 32 + r0;
+  for (int i = 0; i < kTileRows * kTileCols / 16 / kRepackThreads; ++i) {
+    const int idx = t + i * kRepackThreads;
+    const int row = idx >> 3, chunk = idx & 7;
+    const int r = rm * kTileRows + row;
+    const int c = c_base + chunk * 16;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (r < rows && c < cols) {
+      const uint8_t* src = sf + (l * rows + r) * static_cast<long long>(cols) + c;
+      if (vec) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+      } else if (words) {
 #pragma unroll
-    for (int j = 0; j < kAtomsPerThread; ++j) w[r1][j] = 0u;
-    if (r >= rows) continue;
-    const uint8_t* src = sf + (l * rows + r) * static_cast<long long>(cols) + c0;
-    if (wide) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-      w[r1][0] = a.x; w[r1][1] = a.y; w[r1][2] = a.z; w[r1][3] = a.w;
-      w[r1][4] = b.x; w[r1][5] = b.y; w[r1][6] = b.z; w[r1][7] = b.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < kAtomsPerThread; ++j) {
-        const int c = c0 + 4 * j;
-        if (c >= cols) break;
-        if (aligned_cols) {
-          w[r1][j] = __ldg(reinterpret_cast<const uint32_t*>(src + 4 * j));
-        } else {
-          uint32_t v = 0;
-          for (int cc = 0; cc < 4 && c + cc < cols; ++cc) v |= static_cast<uint32_t>(src[4 * j + cc]) << (8 * cc);
-          w[r1][j] = v;
-        }
+        for (int e = 0; e < 4; ++e)
+          if (c + 4 * e < cols) w[e] = __ldg(reinterpret_cast<const uint32_t*>(src) + e);
+      } else {
+        for (int b = 0; b < 16 && c + b < cols; ++b) w[b >> 2] |= static_cast<uint32_t>(src[b]) << (8 * (b & 3));
       }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tile[row * kPitchWords + chunk * 4 + e] = w[e];
   }
+  __syncthreads();
+  // store: warp w writes atoms w, w + 8, w + 16, w + 24 of the tile; lane r0
+  // writes the atom's row r0 = the four scales of rows r0, r0+32, r0+64, r0+96
+  const int warp = t >> 5, r0 = t & 31;
   uint4* dst = reinterpret_cast<uint4*>(out) + ((l * rest_m + rm) * rest_k) * 32 + r0;
 #pragma unroll
-  for (int j = 0; j < kAtomsPerThread; ++j) {
-    const int ck = j8 * kAtomsPerThread + j;
-    if (ck < rest_k) dst[static_cast<long long>(ck) * 32] = make_uint4(w[0][j], w[1][j], w[2][j], w[3][j]);
+  for (int i = 0; i < kTileCols / 4 / (kRepackThreads / 32); ++i) {
+    const int a = warp + i * (kRepackThreads / 32);
+    const int ck = ct * (kTileCols / 4) + a;
+    if (ck >= rest_k) break;
+    const uint4 v = make_uint4(tile[r0 * kPitchWords + a], tile[(r0 + 32) * kPitchWords + a],
+                               tile[(r0 + 64) * kPitchWords + a], tile[(r0 + 96) * kPitchWords + a]);
+    dst[static_cast<long long>(ck) * 32] = v;
   }
 }
 
@@ -77,15 +82,12 @@ cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cud
   const int cols = K / 16;
   const int rest_m = (rows + 127) / 128;
   const int rest_k = ((K + 255) / 256) * 4;
-  const int groups = (rest_k + kAtomsPerThread - 1) / kAtomsPerThread;
-  const long long work = static_cast<long long>(L) * rest_m * groups * 32;
-  if (work == 0) return cudaSuccess;
-  const int threads = 256;
-  const long long blocks = (work + threads - 1) / threads;
+  const int ctiles = (rest_k + kTileCols / 4 - 1) / (kTileCols / 4);
+  const long long blocks = static_cast<long long>(L) * rest_m * ctiles;
+  if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  repack_scales_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, cols, rest_m, rest_k,
-      work);
+  repack_scales_kernel<<<static_cast<unsigned>(blocks), kRepackThreads, 0, stream>>>(
+      static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, cols, rest_m, rest_k, ctiles);
   return cudaGetLastError();
 }
 

@@ -141,6 +141,16 @@ NVFP4_API int nvfp4_gemm_run(const void* A, const void* B, const void* SFA, cons
  *                    nvfp4_gemm_run
  *   M, N, K, L       host arrays of G sizes, per group as in nvfp4_gemm_run
  * Errors: as nvfp4_gemm_run; the first offending group is named.
+ *
+ * Workspace: plans whose tiles are summed from partial results in a device
+ * workspace (nvfp4_gemm_plan out[7] > 1 and out[10] == 0) use one per device
+ * and stream, created by the first such launch and grown (at least doubled)
+ * by a launch that needs more; growing synchronises the stream and is an
+ * INVALID_ARG error while the stream is being captured into a CUDA graph
+ * (run the problem once on the stream before capturing it).  A replaced
+ * buffer stays allocated until the process exits, so a graph captured
+ * before the growth stays valid.  Launches that share a workspace must not
+ * run concurrently: replay such graphs on the stream they were captured on.
  */
 NVFP4_API int nvfp4_gemm_run_grouped(int G, const void* const* A, const void* const* B,
                            const void* const* SFA, const void* const* SFB, void* const* C,

@@ -12,6 +12,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("rows,K,L", [
     (128, 256, 1), (1, 256, 1), (200, 512, 1), (7168, 16384, 1), (130, 768, 3),
     (64, 320, 2), (1000, 1024, 1), (96, 48, 1), (300, 1088, 2), (7, 8192, 1), (129, 4352, 1),
+    (100, 1040, 2), (257, 33024, 1),
 ])
 def test_repack_matches_oracle(rows, K, L):
     binding = require_gpu()
