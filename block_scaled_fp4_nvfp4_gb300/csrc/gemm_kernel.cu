@@ -53,7 +53,6 @@ struct SmemCtl {
   uint64_t epi_bcast;
   uint64_t mma_drain;
   uint64_t red_go;    // cluster reduction: every CTA of the cluster may now be written
-  uint64_t red_staged;  // cluster reduction: every epilogue warp's staging slots written
   uint64_t red_full;    // cluster reduction: every peer's slice of this CTA's columns landed
   uint64_t part_full;   // pair stream-K: the other segment's partial landed in the ring
   uint32_t tmem_base;
@@ -63,13 +62,14 @@ struct SmemCtl {
   // stage, the last use (the warp's k-tile count) it issued copies for and
   // the bytes those copies deliver to each destination barrier; warp 0's
   // arming of each stage (use and armed byte count); in reduce clusters,
-  // whether red_full was armed and which ranks this CTA's partial went to.
+  // whether red_full was armed and, per epilogue warp, which ranks its part
+  // of this CTA's partial went to.
   int rec_use[kProducerWarps][kMaxStages];
   uint32_t rec_bytes[kProducerWarps][kMaxStages];
   int arm_use[kMaxStages];
   uint32_t arm_bytes[kMaxStages];
   int red_armed;
-  uint32_t red_sent;
+  uint32_t red_sent[kEpiWarps];  // per epilogue warp: ranks its part of the partial went to
   uint32_t part_armed;   // bytes part_full was armed with
   uint32_t part_issued;  // bytes of partial copies issued
   uint32_t peer_abort[4];  // abort flags the cluster's CTAs published here (index = rank)
@@ -201,7 +201,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     ptx::mbar_init(ptx::smem_addr(&ctl.epi_bcast), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl.mma_drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl.red_go), CL);                 // one arrival per CTA of the cluster
-    ptx::mbar_init(ptx::smem_addr(&ctl.red_staged), kEpiWarps);
     ptx::mbar_init(ptx::smem_addr(&ctl.red_full), 1);  // armed with the peers' bytes
     ptx::mbar_init(ptx::smem_addr(&ctl.part_full), 1);
     ctl.abort = 0;
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       ctl.arm_bytes[s] = 0;
     }
     ctl.red_armed = 0;
-    ctl.red_sent = 0;
+    for (int w = 0; w < kEpiWarps; ++w) ctl.red_sent[w] = 0;
     ctl.part_armed = 0;
     ctl.part_issued = 0;
     for (int r = 0; r < 4; ++r) ctl.peer_abort[r] = 0;
@@ -333,9 +332,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     }
     if constexpr (kRed) {
       constexpr uint32_t kSlotBytes = BN / CL * kBM * 4;
-      uint32_t got = 0;
+      constexpr uint32_t kWarpPart = kSlotBytes / kEpiWarps;
+      uint32_t got = 0;  // bytes the peers' warps sent into this CTA's receive slots
       for (int r = 0; r < CL; ++r)
-        if (r != crank && ((peer_word(&ctl.red_sent, r) >> crank) & 1u)) got += kSlotBytes;
+        if (r != crank)
+          for (int w = 0; w < kEpiWarps; ++w)
+            if ((peer_word(&ctl.red_sent[w], r) >> crank) & 1u) got += kWarpPart;
       const uint32_t bar = ptx::smem_addr(&ctl.red_full);
       if ((ctl.red_armed || got) && !ptx::mbar_try_wait(bar, 0)) {
         const uint32_t expected = (CL - 1) * kSlotBytes;
@@ -867,15 +869,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
         // = segment) and each CTA reduces and stores BN/CL of the columns.
         // The operand ring, idle once a CTA's only work item is done, holds
         // CL receive slots (slot j: segment j's fp32 partial of this CTA's
-        // columns, as [BN/CL/4][128 rows][4]) and then CL staging slots
-        // (staging slot r: this CTA's partial of rank r's columns).  Every
-        // thread drains its row into its own receive slot and the staging
-        // slots; one thread bulk-copies each staging slot into its owner's
-        // receive slot, where the owner's red_full barrier counts the bytes;
-        // the owner sums the CL slots in segment (= k) order, as the
-        // workspace path does.  Each thread reads back only its own row.
+        // columns) and then CL staging slots (staging slot r: this CTA's
+        // partial of rank r's columns).  A slot is laid out by epilogue warp:
+        // [warp][column / 4][row % 32][4 floats], so each warp's 32 rows are
+        // one contiguous part of kSlotBytes / 4.  Every warp drains its rows
+        // into its own receive slot and the staging slots -- the other ranks'
+        // columns first -- and, once every CTA of the cluster is idle, bulk-
+        // copies its part of each staging slot into the owner's receive slot,
+        // where the owner's red_full barrier counts the bytes; the warps'
+        // copies run side by side and overlap the draining of the CTA's own
+        // columns.  The owner sums the CL slots in segment (= k) order, as
+        // the workspace path does.  Each thread reads back only its own row.
         constexpr int kOwnCols = BN / CL;
         constexpr uint32_t kSlotBytes = kOwnCols * kBM * 4;
+        constexpr uint32_t kWarpPart = kSlotBytes / kEpiWarps;
         static_assert(kOwnCols % 32 == 0, "whole 32-column boxes per CTA");
         static_assert(2 * CL * kSlotBytes + kEpiWarps * (kOwnCols / 32) * Cfg::kEpiBufBytes <= kStages * Cfg::kStageBytes,
                       "reduction slots and C staging exceed the ring");
@@ -888,7 +895,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           break;
         }
         const uint32_t go_bar = ptx::smem_addr(&ctl.red_go);
-        const uint32_t staged_bar = ptx::smem_addr(&ctl.red_staged);
         const uint32_t rfull_bar = ptx::smem_addr(&ctl.red_full);
         // This CTA's MMAs are complete (acc_full), so its ring may be
         // written: tell every CTA of the cluster.
@@ -897,42 +903,54 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           ptx::mbar_arrive_expect_tx(rfull_bar, (CL - 1) * kSlotBytes);
           ctl.red_armed = 1;
         }
-        uint32_t slot[CL];
+        // receive slot of this CTA's columns, staging slot of rank r's
+        auto slot_of = [&](int r) {
+          return smem_base + static_cast<uint32_t>(r == static_cast<int>(crank) ? r : CL + r) * kSlotBytes;
+        };
+        const uint32_t part = static_cast<uint32_t>(sub) * kWarpPart + static_cast<uint32_t>(lane) * 16;
+        bool sent_ok = true;
+        auto send_parts = [&]() {
+          // every lane's staging stores visible to the bulk copies, every
+          // CTA of the cluster idle, then one copy per other rank
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (!warp_wait<true>(W, go_bar, 0, kStatusTimeoutEpilogue)) {
+            sent_ok = false;
+            return;
+          }
+          if (lane == 0) {
 #pragma unroll
-        for (int r = 0; r < CL; ++r)
-          slot[r] = smem_base + static_cast<uint32_t>(r == static_cast<int>(crank) ? r : CL + r) * kSlotBytes + row * 16;
+            for (int r = 0; r < CL; ++r)
+              if (r != static_cast<int>(crank)) {
+                ptx::bulk_copy_to_cluster(
+                    ptx::mapa_shared(smem_base + crank * kSlotBytes + sub * kWarpPart, static_cast<uint32_t>(r)),
+                    smem_base + static_cast<uint32_t>(CL + r) * kSlotBytes + sub * kWarpPart, kWarpPart,
+                    ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
+                ctl.red_sent[sub] |= 1u << r;
+              }
+          }
+          __syncwarp();
+        };
+        // 64-column chunks, the other ranks' first: with two ranks, the
+        // peer's half is sent while this CTA's own half is drained
+        constexpr int kChunks = BN / 64;
 #pragma unroll
-        for (int q = 0; q < BN / 64; ++q) {
+        for (int qi = 0; qi < kChunks; ++qi) {
+          const int q = CL == 2 ? (qi + (crank == 0 ? 1 : 0)) % kChunks : qi;
           float v[64];
           load_chunk(t_row + 64 * q, v);
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const int col = 64 * q + 4 * c4;
-            st_shared_v4(slot[col / kOwnCols] + (col % kOwnCols) / 4 * (kBM * 16), __float_as_uint(v[4 * c4]),
+            st_shared_v4(slot_of(col / kOwnCols) + part + (col % kOwnCols) / 4 * 512, __float_as_uint(v[4 * c4]),
                          __float_as_uint(v[4 * c4 + 1]), __float_as_uint(v[4 * c4 + 2]),
                          __float_as_uint(v[4 * c4 + 3]));
           }
+          if (CL == 2 && qi == 0) send_parts();
         }
         release_acc();
-        ptx::fence_proxy_async_smem();  // the staging slots are read by bulk copies
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(staged_bar);
-        if (ew == 0) {
-          // every warp's staging written and every CTA of the cluster idle
-          if (!warp_wait(W, staged_bar, 0, kStatusTimeoutEpilogue)) break;
-          if (!warp_wait<true>(W, go_bar, 0, kStatusTimeoutEpilogue)) break;
-          if (lane == 0) {
-#pragma unroll
-            for (int r = 0; r < CL; ++r)
-              if (r != static_cast<int>(crank)) {
-                ptx::bulk_copy_to_cluster(ptx::mapa_shared(smem_base + crank * kSlotBytes, static_cast<uint32_t>(r)),
-                                          smem_base + static_cast<uint32_t>(CL + r) * kSlotBytes, kSlotBytes,
-                                          ptx::mapa_shared(rfull_bar, static_cast<uint32_t>(r)));
-                ctl.red_sent |= 1u << r;
-              }
-          }
-          __syncwarp();
-        }
+        if (CL != 2) send_parts();
+        if (!sent_ok) break;
         if (!warp_wait(W, rfull_bar, 0, kStatusTimeoutEpilogue)) break;
 #pragma unroll
         for (int cg = 0; cg < kOwnCols / 32; ++cg) {
@@ -943,7 +961,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           for (int j = 0; j < CL; ++j)
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 t = ld_shared_v4(smem_base + j * kSlotBytes + ((cg * 8 + c4) * kBM + row) * 16);
+              const float4 t = ld_shared_v4(smem_base + j * kSlotBytes + part + (cg * 8 + c4) * 512);
               acc[c4].x += t.x;
               acc[c4].y += t.y;
               acc[c4].z += t.z;
