@@ -371,6 +371,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     int count = 0;
     bool ok = true;
     bool dep_done = false;  // griddepcontrol.wait passed
+    const int skip_at = blockIdx.x == 0 ? p.debug_skip_ktile : -1;
+    const uint32_t full0 = full_bar(0), empty0 = empty_bar(0);
+    [[maybe_unused]] uint32_t lfull0 = 0;
+    if constexpr (P2) lfull0 = ptx::mapa_shared(full0, 0);
     WorkCursor cur;
     work_begin(p.sched, unit, units, cur, wrank);
     Work x;
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       const uint32_t stage_tx =
           Cfg::kABytes + Cfg::kBBytes + kSfSlabBytes + static_cast<uint32_t>(nsfb) * kSfSlabBytes;
       for (int kt = x.kt0; kt < x.kt1; ++kt) {
-        if (!warp_wait(W, empty_bar(stage), phase ^ 1u, kStatusTimeoutProducer)) {
+        if (!warp_wait(W, empty0 + 8u * stage, phase ^ 1u, kStatusTimeoutProducer)) {
           ok = false;
           break;
         }
@@ -407,17 +411,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
           ptx::griddep_wait();  // the previous kernel's writes are visible from here on
           dep_done = true;
         }
-        if (blockIdx.x == 0 && count == p.debug_skip_ktile) {
+        if (count == skip_at) {
           // test-only: nothing issued, nothing in flight, nothing recorded
         } else {
-          const uint32_t fb = full_bar(stage);
+          const uint32_t fb = full0 + 8u * stage;
           if constexpr (P2) {
             // Every copy of both CTAs lands on the leader's barrier, armed by
             // the leader with both CTAs' bytes.  Both B scale slabs go to each
             // CTA (each tensor core scales all BN columns); a slab past the
             // last 128-row block reads other scales or zeros, harmless since
             // those B rows are zero-filled and their columns are not stored.
-            const uint32_t lfb = ptx::mapa_shared(fb, 0);
+            const uint32_t lfb = lfull0 + 8u * stage;
             if (warp == 0) {
               if (crank == 0) ptx::mbar_arrive_expect_tx_elect(fb, 2u * Cfg::kStageBytes);
               ptx::tma_load_3d_pair_elect(sA, mapA, kt * kBKBytes, x.tm * kBM, x.l, lfb, polA);
@@ -562,6 +566,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
     constexpr uint64_t kKbStep = 32 >> 4;  // 64 E2M1 codes = 32 bytes per row per MMA
     static_assert(Cfg::kDynSmem + 2048 < (1 << 18), "shared addresses fit the 14-bit descriptor field");
     const uint32_t sf_tmem0 = tmem + Cfg::kSfBaseCol;
+    const uint32_t mfull0 = full_bar(0), mempty0 = empty_bar(0);
     int stage = 0;
     uint32_t phase = 0;
     int ab = 0;
@@ -582,7 +587,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
       // ("nvfp4 group gemm, submission 407526": sfb_lane).
       const uint32_t sfb_col0 = BN < 128 ? static_cast<uint32_t>((x.tn * BN) % 128 / 32) : 0u;
       for (int kt = x.kt0; kt < x.kt1; ++kt) {
-        if (!warp_wait(W, full_bar(stage), phase, kStatusTimeoutMma)) {
+        if (!warp_wait(W, mfull0 + 8u * stage, phase, kStatusTimeoutMma)) {
           ok = false;
           break;
         }
@@ -610,11 +615,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) nvfp4_gemm_kernel(const __grid
               dB + kb * kKbStep, idesc, sfa_t + 4 * kb, sfb_t + kb * Cfg::kSfbKbCols + sfb_col0, acc);
         }
         if constexpr (P2)
-          ptx::tc_commit2_mc_elect(empty_bar(stage), kPeers);  // the stage is free in both CTAs
+          ptx::tc_commit2_mc_elect(mempty0 + 8u * stage, kPeers);  // the stage is free in both CTAs
         else if constexpr (!kMc)
-          ptx::tc_commit_elect(empty_bar(stage));
+          ptx::tc_commit_elect(mempty0 + 8u * stage);
         else
-          ptx::tc_commit_mc_elect(empty_bar(stage), kPeers);  // the stage is free once both CTAs read it
+          ptx::tc_commit_mc_elect(mempty0 + 8u * stage, kPeers);  // the stage is free once both CTAs read it
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
