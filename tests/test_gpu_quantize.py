@@ -77,3 +77,30 @@ def test_quantized_operands_through_the_gemm():
     cb, sb = oracle.quantize(b, N, K)
     assert_close_full(C, dict(A=ca, B=cb, SFA=sa, SFB=sb, M=M, N=N, K=K, L=1))
     check_canary(buf, M, N, 1)
+
+
+def test_quantize_full_size_sampled_rows():
+    """The bench's quantize leg at full size (7168 x 16384 bf16, one launch in
+    the launch configuration bench.py times): codes and scales of 48 sampled
+    rows (block edges, the last row, random ones) byte for byte against the
+    oracle's quantization of those rows.  Scales are read back from the atom
+    layout by its definition: byte (r, c) of the row-major scales sits at
+    ((r/128)*(K/64) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4."""
+    binding = require_gpu()
+    L, rows, K = 1, 7168, 16384
+    g = torch.Generator().manual_seed(20261203)
+    x = (torch.randn((L, rows, K), generator=g) *
+         torch.exp2(torch.randint(-8, 9, (L, rows, 1), generator=g).float())).to(torch.bfloat16)
+    codes, sf = binding.quantize(x.cuda())
+    torch.cuda.synchronize()
+    pick = sorted(set([0, 1, 31, 32, 127, 128, 129, 3583, 3584, 7039, 7040, 7167] +
+                      torch.randint(0, rows, (36,), generator=g).tolist()))
+    sel = torch.tensor(pick)
+    ref_codes, ref_sf = oracle.quantize(x[:, sel, :], len(pick), K, L)
+    got_codes = codes[0, sel.cuda(), :].cpu().numpy()
+    assert np.array_equal(got_codes, ref_codes[0]), "codes differ"
+    flat = sf.cpu().numpy()
+    r = np.asarray(pick)[:, None]
+    c = np.arange(K // 16)[None, :]
+    off = ((r // 128) * (K // 64) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+    assert np.array_equal(flat[off], ref_sf[0]), "scales differ"
