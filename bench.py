@@ -69,6 +69,9 @@ def parse(argv=None):
     ap.add_argument("--check", action="store_true", help="oracle check of set 0 (sampled)")
     ap.add_argument("--no-quantize", action="store_true", help="skip the fused quantize + repack leg")
     ap.add_argument("--no-repack-step", action="store_true", help="skip the step_with_repack leg")
+    ap.add_argument("--clock-window-s", type=float, default=1.0,
+                    help="seconds of untimed back-to-back steps after each timed region, sampled for the "
+                         "clock record (0: sample the timed region only)")
     return ap.parse_args(argv)
 
 
@@ -157,11 +160,13 @@ class ClockSampler:
                 continue
         os.unlink(self.path)
 
-    def window(self, t0, t1):
+    def window(self, t0, t1, margin=0.05, label="timed"):
+        """Samples taken within [t0 - margin, t1 + margin] (a negative margin
+        trims the ends)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        inside = [r for r in self.rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
-        window = "timed"
+        inside = [r for r in self.rows if t0 - margin <= r[0] <= t1 + margin]
+        window = label
         if not inside:
             inside = sorted(self.rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
             window = "adjacent (timed region %.4f s, shorter than the 0.1 s sampling period)" % (t1 - t0)
@@ -407,6 +412,24 @@ def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
     host0, dev_sets = device_inputs(binding, wl, sets, dev)
     elapsed_ms, tw0, tw1 = time_launches(binding, dev_sets, args.steps, args.warmup, stream, flush)
     launch = binding.nvfp4_gemm_last_launch()
+    # The timed region is mostly far shorter than nvidia-smi's 100 ms sampling
+    # period, so its samples can miss the load.  For the clock record the same
+    # steps then run back to back, untimed, for about --clock-window-s seconds
+    # while the sampler keeps running.
+    # Chunks of about a quarter second of device time (K steps where every
+    # step also flushes L2), until the window's wall time is reached.
+    load_wall = None
+    if args.clock_window_s > 0:
+        per_step = max(elapsed_ms / args.steps * 1e-3, 1e-6)
+        chunk = args.steps if flush is not None else int(min(100000, max(args.steps, math.ceil(0.25 / per_step))))
+        n = 0
+        lw0 = time.time()
+        while True:
+            time_launches(binding, dev_sets, chunk, 0, stream, flush)
+            n += chunk
+            if time.time() - lw0 >= args.clock_window_s:
+                break
+        load_wall = (lw0, time.time(), n)
     launch_s = elapsed_ms / args.steps * 1e-3
     bound, t_hbm, t_fp4, hbm, fp4 = roofline_terms(wl, peaks)
     if bound == "hbm":
@@ -431,6 +454,7 @@ def measure_workload(binding, name, args, dev, stream, l2, peaks, peak_src):
                      "frac_of_size_matched_copy": None if copy_ref is None else achieved / copy_ref["achieved"]},
         "roofline_fraction_min_time": max(t_hbm, t_fp4) / launch_s,
         "_wall": (tw0, tw1),
+        "_load_wall": load_wall,
     }
     del flush
     if args.check:
@@ -660,9 +684,21 @@ def main(argv=None):
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": desc + ", %.1f s" % dt}
 
-    # clocks of each timed region (the sampler ran across all of them)
+    # clocks of each workload (the sampler ran across every timed region and
+    # every back-to-back window): the back-to-back window's samples, the first
+    # and last 50 ms left out, where there is one; the timed region's beside it
     for res in per_config.values():
-        res["clocks"] = sampler.window(*res.pop("_wall"))
+        timed = sampler.window(*res.pop("_wall"))
+        load = res.pop("_load_wall")
+        if load is None:
+            res["clocks"] = timed
+            continue
+        lw0, lw1, n = load
+        clocks = sampler.window(lw0, lw1, margin=-0.05,
+                                label="%d untimed back-to-back steps (%.2f s) right after the timed ones"
+                                      % (n, lw1 - lw0))
+        clocks["timed_region"] = timed
+        res["clocks"] = clocks
     line = {
         "metric": METRIC, "value": head["tflops"], "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["us_per_launch"] / 1e3, "higher_is_better": True,
