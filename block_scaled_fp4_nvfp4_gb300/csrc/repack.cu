@@ -17,6 +17,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace nvfp4 {
 
 constexpr int kTileRows = 128;   // one 128-row scale block
@@ -29,6 +31,12 @@ __global__ void __launch_bounds__(kRepackThreads) repack_scales_kernel(const uin
                                                                        int cols, int rest_m, int rest_k,
                                                                        int ctiles) {
   __shared__ uint32_t tile[kTileRows * kPitchWords];
+  // Programmatic dependent launch: the next kernel on the stream may be
+  // scheduled now, and this grid may have started before the previous kernel
+  // finished, so it waits for it before touching global memory (the previous
+  // kernel may produce `sf` or still read `out`).
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   // block = (l * rest_m + rm) * ctiles + ct
   const int ct = static_cast<int>(blockIdx.x % static_cast<unsigned>(ctiles));  // atoms 32*ct .. 32*ct+31
   const long long lm = blockIdx.x / static_cast<unsigned>(ctiles);
@@ -86,9 +94,20 @@ cudaError_t repack_launch(const void* sf, void* out, int rows, int K, int L, cud
   const long long blocks = static_cast<long long>(L) * rest_m * ctiles;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  repack_scales_kernel<<<static_cast<unsigned>(blocks), kRepackThreads, 0, stream>>>(
-      static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out), rows, cols, rest_m, rest_k, ctiles);
-  return cudaGetLastError();
+  // launched like the GEMM, as a programmatic dependent of the previous kernel
+  // on the stream: back-to-back launches overlap one's start with the other's end
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kRepackThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, repack_scales_kernel, static_cast<const uint8_t*>(sf), static_cast<uint8_t*>(out),
+                            rows, cols, rest_m, rest_k, ctiles);
 }
 
 }  // namespace nvfp4
