@@ -38,6 +38,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace nvfp4 {
 
 namespace {
@@ -118,6 +120,11 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const uint16_t* _
     const float dv = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3)));
     scale_tab[c] = make_float2(dv, c != 0 ? __frcp_rn(dv) : 0.0f);
   }
+  // Programmatic dependent launch: the table above overlaps the previous
+  // kernel on the stream; global memory waits for it (it may produce x or
+  // still read the codes and scales about to be overwritten).
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   __syncthreads();
   const int lane = threadIdx.x & 31;
   uint8_t* atom = atoms[threadIdx.x >> 5];
@@ -205,13 +212,19 @@ cudaError_t quantize_launch(const void* x, int is_f16, void* codes, void* sf, in
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* c = static_cast<uint8_t*>(codes);
   uint8_t* s = static_cast<uint8_t*>(sf);
-  if (is_f16)
-    quantize_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
-                                                                                  atoms_per_block);
-  else
-    quantize_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(xs, c, s, rows, K, L, row_blocks,
-                                                                                   atoms_per_block);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel on the stream, like the GEMM
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (is_f16) return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, xs, c, s, rows, K, L, row_blocks, atoms_per_block);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<false>, xs, c, s, rows, K, L, row_blocks, atoms_per_block);
 }
 
 }  // namespace nvfp4

@@ -29,10 +29,10 @@
  *     NVFP4_ERR_INVALID_ARG before anything is launched.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  All work is asynchronous on that stream; nothing synchronises
- *     unless stated.  The GEMM and repack kernels are launched as programmatic
- *     dependents of the work before them on the stream: they may be scheduled
- *     while that work drains, but touch no global memory until it has
- *     completed, so stream order holds as for any kernel.
+ *     unless stated.  The GEMM, repack and quantize kernels are launched as
+ *     programmatic dependents of the work before them on the stream: they may
+ *     be scheduled while that work drains, but touch no global memory until
+ *     it has completed, so stream order holds as for any kernel.
  *   - Return value: NVFP4_OK or a negative nvfp4_status.  On error nothing is
  *     queued, and nvfp4_gemm_last_error_string() (per calling thread) says why.
  *     The library never aborts the process.
