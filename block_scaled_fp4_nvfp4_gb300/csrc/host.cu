@@ -375,11 +375,12 @@ bool red_allowed() {
 // that runs its first k-tiles last).  NVFP4_PAIR_SK = 1 takes the split
 // minimising the busiest cluster's k-tiles plus kPairSkFixupKtiles for the
 // reduction, 2 forces the smallest valid tail (tests).  Off by default:
-// measured on GB300 (interleaved A/B, one box) the reduction costs about as
-// much SM intake as the balance saves -- the finisher takes in the 128 KB
-// partial (~3.4 k-tiles of intake) and the writer holds its accumulator while
-// it writes one -- 8192^3 166.9 vs 166.9 us, the eight-group MoE workload on
-// padded pairs 52.0 vs 46.5 us.
+// measured on GB300 (interleaved A/B, one box) the reduction costs more SM
+// intake than the balance saves -- the finisher takes in the 128 KB partial
+// (~3.4 k-tiles of intake) and the writer holds its accumulator while it
+// writes one -- 8192^3 158.0-158.8 vs 153.5-154.6 us (431 instead of 448
+// k-tiles on the busiest pair), the eight-group MoE workload on padded pairs
+// 52.0 vs 46.5 us.
 constexpr int kPairSkFixupKtiles = 4;
 
 int pair_sk_mode() {
