@@ -156,12 +156,25 @@ __global__ void __launch_bounds__(kThreads, 3) quantize_kernel(const uint16_t* _
   const long long tasks = static_cast<long long>(L) * row_blocks * atoms_per_block;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const int kblocks = K / 16;
+  const bool small_tasks = tasks <= 0xFFFFFFFFll;
   for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < tasks;
        t += nwarps) {
-    const int kc = static_cast<int>(t % atoms_per_block);  // 64-value chunk = scale atom
-    const long long lrb = t / atoms_per_block;              // batch * row_blocks + row block
-    const int rb = static_cast<int>(lrb % row_blocks);
-    const int l = static_cast<int>(lrb / row_blocks);
+    int kc, rb, l;  // 64-value chunk (= scale atom), 128-row block, batch
+    long long lrb;  // batch * row_blocks + row block
+    if (small_tasks) {  // 32-bit divisions, same quotients (GB300, 7168 x 16384 bf16: 51.6 -> 51.2 us)
+      const uint32_t tt = static_cast<uint32_t>(t);
+      const uint32_t q = tt / static_cast<uint32_t>(atoms_per_block);
+      kc = static_cast<int>(tt - q * static_cast<uint32_t>(atoms_per_block));
+      const uint32_t q2 = q / static_cast<uint32_t>(row_blocks);
+      rb = static_cast<int>(q - q2 * static_cast<uint32_t>(row_blocks));
+      l = static_cast<int>(q2);
+      lrb = q;
+    } else {
+      kc = static_cast<int>(t % atoms_per_block);
+      lrb = t / atoms_per_block;
+      rb = static_cast<int>(lrb % row_blocks);
+      l = static_cast<int>(lrb / row_blocks);
+    }
     const bool kvalid = kc * 4 + b < kblocks;
     // this lane's first row of the block and the 4-row stride, computed once
     // per task instead of a 64-bit row offset per load and store (GB300,
