@@ -2,7 +2,8 @@
 the oracle: a replay computes what an eager launch computes, a graph captured
 before the split-K workspace grew stays valid after it grew (the replaced
 buffer is kept), and a launch that would grow the workspace during capture is
-refused before anything is recorded."""
+refused before anything is recorded.  The preparation kernels (quantize,
+repack) are captured with the GEMM too."""
 import pytest
 import torch
 
@@ -138,3 +139,47 @@ def test_workspace_growth_during_capture_is_refused(monkeypatch):
     torch.cuda.synchronize()
     binding.nvfp4_gemm_check_device_status(stream)
     assert_close_full(C, p)
+
+
+def test_graph_of_quantize_repack_and_gemm():
+    """The whole preparation and the GEMM in one graph: quantize A from bf16,
+    repack B's row-major scales, multiply; three kernels launched as
+    programmatic dependents of one another, replayed twice (outputs cleared
+    in between), against the oracle's quantization and GEMM."""
+    import oracle
+    binding = require_gpu()
+    M, N, K = 256, 512, 2048
+    g = torch.Generator().manual_seed(77)
+    xa = torch.randn((1, M, K), generator=g).to(torch.bfloat16)
+    pb = workloads.make_random_problem(78, M, N, K)
+    stream = torch.cuda.Stream()
+    xa_d = xa.cuda()
+    B = pb["B"].cuda()
+    sfb_raw = pb["SFB"].cuda()
+    codes_a = torch.empty((1, M, K // 2), dtype=torch.uint8, device="cuda")
+    sfa = torch.empty(binding.nvfp4_gemm_repacked_scales_bytes(M, K, 1), dtype=torch.uint8, device="cuda")
+    sfb = torch.empty(binding.nvfp4_gemm_repacked_scales_bytes(N, K, 1), dtype=torch.uint8, device="cuda")
+    buf, C = alloc_c(M, N, 1)
+
+    def step():
+        binding.nvfp4_quantize(xa_d, binding.DTYPE_BF16, codes_a, sfa, M, K, 1, stream)
+        binding.nvfp4_gemm_repack_scales(sfb_raw, sfb, N, K, 1, stream)
+        binding.nvfp4_gemm_run(codes_a, B, sfa, sfb, C, M, N, K, 1, stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    ca, sa = oracle.quantize(xa, M, K)
+    for _ in range(2):
+        for t in (codes_a, sfa, sfb):
+            t.zero_()
+        C.fill_(float("nan"))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        binding.nvfp4_gemm_check_device_status()
+        assert_close_full(C, dict(A=ca, B=pb["B"], SFA=sa, SFB=pb["SFB"], M=M, N=N, K=K, L=1))
+        check_canary(buf, M, N, 1)
